@@ -1,0 +1,207 @@
+/*
+ * pagedkv.h -- C ABI of libpagedkv.so: the paged KV-cache decode hot path on
+ * one GB300 (sm_103a).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Every call returns an int status: PF_OK (0) or one of PF_ERR_*.  On
+ *   failure pf_last_error() gives a message (per calling thread) and nothing
+ *   was launched or changed.
+ * - Device pointers are owned by the caller (e.g. PyTorch tensors); the
+ *   library never allocates or frees device memory.  Host handles
+ *   (pf_pool, pf_alloc) are allocated by *_create and released by *_destroy.
+ * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Device calls are asynchronous on that stream; the caller keeps
+ *   the buffers alive until the work completes.
+ * - Host-visible arguments (null pointers, sizes, 16-byte alignment of
+ *   device buffers, head_dim in {64, 128}, block_size in {1, 16, 64, 256},
+ *   layer in range) are checked before any launch and rejected with
+ *   PF_ERR_INVALID.  Device-resident data (block ids, context lengths,
+ *   positions) cannot be checked on the host: kernels that find a value out
+ *   of range skip that access and record a flag readable with
+ *   pf_device_status(); results for the affected rows are then undefined.
+ * - fp16 is IEEE binary16 (PF_F16); fp32 (PF_F32) is only an output option.
+ *
+ * Pool layout
+ * -----------
+ * K and V are separate pools, each [n_layers][n_blocks][block_size]
+ * [n_kv_heads][head_dim] fp16, row-major ("Why Naive KV-Caches Waste >60%
+ * VRAM", "Implementation Walkthrough": the cache is sized to the physical
+ * pool [N_blocks, block_size, N_heads, D_head]; PageForge, "Five techniques",
+ * 04: all layers stacked in one pool tensor share the block ids).  Token t of
+ * a sequence whose block-table row is `row` lives at slot
+ *     row[t / block_size] * block_size + t % block_size
+ * ("Why Naive KV-Caches Waste >60% VRAM", section 1 "Physical Block Pool &
+ * Block Tables"; PageFault README, "The OS analogy").
+ *
+ * Block tables are int32 [n_seqs][max_blocks_per_seq], row-major; entries
+ * past a sequence's ceil(L / block_size) used blocks are never read.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PF_API __attribute__((visibility("default")))
+#else
+#define PF_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum pf_status {
+    PF_OK = 0,
+    PF_ERR_INVALID = 1,     /* bad argument; nothing launched */
+    PF_ERR_OOM = 2,         /* allocator has fewer free blocks than asked */
+    PF_ERR_DOUBLE_FREE = 3, /* freeing a block that is not allocated */
+    PF_ERR_CUDA = 4,        /* a CUDA runtime call failed (message says which) */
+    PF_ERR_UNSUPPORTED = 5  /* valid but not built (e.g. no sm_103a device) */
+};
+
+enum pf_dtype { PF_F16 = 1, PF_F32 = 2 };
+
+/* Flags in the device status word (pf_device_status). */
+enum pf_device_flag {
+    PF_DEV_BAD_BLOCK_ID = 1,  /* a block id outside [0, n_blocks) was met */
+    PF_DEV_BAD_LENGTH = 2,    /* a context length < 0 or > max_blocks * B */
+    PF_DEV_BAD_POSITION = 4,  /* a write position < 0 or past the table row */
+    PF_DEV_WAIT_TIMEOUT = 8   /* a bounded on-chip wait gave up (kernel bug) */
+};
+
+typedef struct pf_pool pf_pool;
+typedef struct pf_alloc pf_alloc;
+
+/* Message of the last failing call on this thread ("" if none). */
+PF_API const char *pf_last_error(void);
+
+/* ABI version of this header (PF_ABI_VERSION). */
+#define PF_ABI_VERSION 1
+PF_API int pf_abi_version(void);
+
+/* ------------------------------------------------------------- pool ---- */
+
+/* Bytes of ONE of the two pools (K or V) for these dimensions; 0 if a
+ * dimension is not positive or dtype is not PF_F16. */
+PF_API size_t pf_pool_bytes(int n_layers, int n_blocks, int block_size,
+                     int n_kv_heads, int head_dim, int dtype);
+
+/* Describe caller-owned K and V pools (each pf_pool_bytes() bytes of device
+ * memory, 16-byte aligned) as a pool.  Non-owning: destroying the handle
+ * does not free the memory.  The handle caches TMA descriptors for the
+ * current device.  dtype must be PF_F16; head_dim 64 or 128; block_size 1,
+ * 16, 64 or 256.  Source: PageForge "Four layers, one pointer" (one pool
+ * tensor of shape (N_pages, page_size, n_layers x n_heads, d_head)). */
+PF_API int pf_pool_create(pf_pool **out, void *k_base, void *v_base, int n_layers,
+                   int n_blocks, int block_size, int n_kv_heads, int head_dim,
+                   int dtype);
+PF_API int pf_pool_destroy(pf_pool *pool);
+
+/* -------------------------------------------------- host allocator ---- */
+/* O(1) free-list allocator over block ids [0, n_blocks).  A LIFO stack
+ * ("Why Naive KV-Caches Waste >60% VRAM", "Implementation Walkthrough":
+ * stack initialised so block 0 comes out first; pop to allocate, append to
+ * free).  shuffle_seed != 0 permutes the initial hand-out order with a
+ * Fisher-Yates shuffle driven by SplitMix64 (what a pool looks like after
+ * churn, PageFault README "Four stages"); 0 keeps 0, 1, 2, ...
+ * Host memory only; not thread-safe (one owner thread). */
+PF_API int pf_alloc_create(pf_alloc **out, int n_blocks, uint64_t shuffle_seed);
+PF_API int pf_alloc_destroy(pf_alloc *a);
+/* Pop n block ids into ids_out[0..n).  All-or-nothing: PF_ERR_OOM and no
+ * change if fewer than n are free (PageFault README "Test"). */
+PF_API int pf_alloc_blocks(pf_alloc *a, int n, int32_t *ids_out);
+/* Push n ids back (ids[0] first, so ids[n-1] is handed out next).  Every id
+ * is checked first: one that is out of range, not allocated, or repeated in
+ * the list gives PF_ERR_DOUBLE_FREE and no change. */
+PF_API int pf_free_blocks(pf_alloc *a, const int32_t *ids, int n);
+/* Number of free blocks, or -1 for a null handle. */
+PF_API int pf_alloc_free_count(const pf_alloc *a);
+/* Demand paging (PagedAttention blog, "Architecture"): grow one sequence
+ * from cur_len to new_len tokens, appending ceil(new_len/B) - ceil(cur_len/B)
+ * fresh blocks to table_row (host int32, max_blocks entries).  Tokens go into
+ * the last block while it has room.  All-or-nothing (PF_ERR_OOM, row and
+ * allocator unchanged); PF_ERR_INVALID if the row is too short or
+ * new_len < cur_len. */
+PF_API int pf_seq_reserve(pf_alloc *a, int block_size, int32_t *table_row,
+                   int max_blocks, int cur_len, int new_len);
+/* Free the ceil(len/B) blocks of a finished sequence (PageForge: pages are
+ * returned the moment a sequence finishes). */
+PF_API int pf_seq_release(pf_alloc *a, int block_size, const int32_t *table_row,
+                   int len);
+
+/* ---------------------------------------------------- device calls ---- */
+
+/* Scatter (PageForge, "Four layers, one pointer": scatter_kv_layer writes
+ * new tokens back into their pages).  Token i of the batch belongs to
+ * sequence seq_idx[i] (a row of block_tables, which has n_table_rows rows of
+ * max_blocks_per_seq entries) at logical position pos[i]; its rows
+ * k_new[i][0..Hkv)[0..D) and v_new[i][..] (fp16, [n_tokens][Hkv][D],
+ * contiguous, device) are copied to its slot of layer `layer`.  One launch
+ * covers all tokens and heads.  block_tables, seq_idx, pos: device int32.
+ * Two tokens of one call must not target the same slot.  Bit-exact copy.
+ * n_tokens == 0 is a no-op. */
+PF_API int pf_write_kv(const pf_pool *pool, int layer, const void *k_new,
+                const void *v_new, const int32_t *block_tables,
+                int n_table_rows, int max_blocks_per_seq,
+                const int32_t *seq_idx, const int32_t *pos, int n_tokens,
+                void *stream);
+
+/* Gather (PageForge, "Four layers, one pointer": gather_kv assembles a
+ * sequence's scattered pages into a contiguous buffer).  For every sequence
+ * s and t < context_lens[s], row cu_off[s] + t of k_out / v_out
+ * ([rows][Hkv][D] fp16, device) receives token t of layer `layer`.
+ * context_lens: device int32 [n_seqs]; cu_off: device int64 [n_seqs]
+ * (row offsets; the caller sizes the outputs).  Bit-exact copy. */
+PF_API int pf_gather_kv(const pf_pool *pool, int layer, const int32_t *block_tables,
+                 int max_blocks_per_seq, const int32_t *context_lens,
+                 const int64_t *cu_off, int n_seqs, void *k_out, void *v_out,
+                 void *stream);
+
+/* Workspace bytes pf_paged_decode_attention needs for a batch of n_seqs
+ * sequences of at most max_blocks_per_seq * block_size tokens with
+ * n_q_heads query heads and this split setting.  0 on bad arguments. */
+PF_API size_t pf_decode_workspace_bytes(const pf_pool *pool, int n_seqs,
+                                 int n_q_heads, int max_blocks_per_seq,
+                                 int split_tokens);
+
+/* Prepare a workspace for first use (zero its counters).  Needed once after
+ * the workspace is allocated, and again after a call whose device status
+ * reported PF_DEV_WAIT_TIMEOUT.  Successful attention calls leave it ready. */
+PF_API int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stream);
+
+/* Single-query decode attention through the block tables (PagedAttention
+ * blog, "The Attention Kernel").  For each sequence s and q-head hq, with
+ * L = context_lens[s] and kv-head h = hq / (n_q_heads / Hkv):
+ *   z_t = scale * sum_d q[s][hq][d] * K[slot(s, t)][h][d],  t < L
+ *   out[s][hq][d] = sum_t softmax(z)_t * V[slot(s, t)][h][d]
+ * fp32 accumulation; L = 0 gives zeros.  q: fp16 [n_seqs][n_q_heads][D];
+ * out: [n_seqs][n_q_heads][D] of out_dtype (PF_F16, rounded to nearest even,
+ * or PF_F32); n_q_heads must be a multiple of Hkv (grouped heads share one
+ * page load).  Sequences longer than split_tokens are cut into chunks whose
+ * partial results are combined with the log-sum-exp rule (same section:
+ * reduction across thread blocks); split_tokens 0 = choose automatically,
+ * -1 = never split, > 0 = chunk length (rounded up to a multiple of 16).
+ * workspace: device memory of at least pf_decode_workspace_bytes(...) bytes,
+ * initialised once with pf_decode_workspace_init; calls sharing a workspace
+ * must not overlap on the GPU. */
+PF_API int pf_paged_decode_attention(const pf_pool *pool, int layer, const void *q,
+                              const int32_t *block_tables,
+                              int max_blocks_per_seq,
+                              const int32_t *context_lens, int n_seqs,
+                              int n_q_heads, float scale, void *out,
+                              int out_dtype, int split_tokens,
+                              void *workspace, size_t ws_bytes, void *stream);
+
+/* Read the device status word (OR of pf_device_flag bits set by kernels of
+ * this library on the current device since the last reset) into *status_out.
+ * Synchronises `stream`.  reset != 0 clears the word afterwards. */
+PF_API int pf_device_status(int *status_out, int reset, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

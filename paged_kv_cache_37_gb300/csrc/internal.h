@@ -1,0 +1,108 @@
+// internal.h -- declarations shared by the host C++ and the CUDA launchers of
+// libpagedkv.so.  Not part of the public ABI (include/pagedkv.h is).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+#include <mutex>
+#include <string>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+// Thread-local last-error message; set_error returns the status it is given.
+int set_error(int status, const std::string &msg);
+int cuda_error(cudaError_t err, const char *what);
+void clear_error();
+
+// Maximum devices a pool caches descriptors for.
+constexpr int kMaxDevices = 64;
+
+// Tile height (tokens) the attention kernel stages per TMA transaction.
+constexpr int kTileTokens = 16;
+
+}  // namespace pkv
+
+// Non-owning description of caller-owned K and V pools.
+struct pf_pool {
+    void *k_base;
+    void *v_base;
+    int n_layers;
+    int n_blocks;
+    int block_size;
+    int n_kv_heads;
+    int head_dim;
+    int dtype;
+    // TMA descriptors over K and V viewed as [rows][n_kv_heads][head_dim]
+    // with rows = n_layers * n_blocks * block_size, encoded lazily per device.
+    std::mutex mu;
+    bool tmap_ready[pkv::kMaxDevices];
+    CUtensorMap tmap_k[pkv::kMaxDevices];
+    CUtensorMap tmap_v[pkv::kMaxDevices];
+};
+
+namespace pkv {
+
+// Device status word of the current device (a __device__ variable of this
+// library); kernels OR pf_device_flag bits into it.
+int *device_status_ptr();
+
+int encode_pool_tmaps(pf_pool *pool, int device);
+
+struct WriteArgs {
+    const pf_pool *pool;
+    int layer;
+    const void *k_new;
+    const void *v_new;
+    const int32_t *block_tables;
+    int n_table_rows;
+    int max_blocks;
+    const int32_t *seq_idx;
+    const int32_t *pos;
+    int n_tokens;
+};
+int launch_write_kv(const WriteArgs &a, cudaStream_t stream);
+
+struct GatherArgs {
+    const pf_pool *pool;
+    int layer;
+    const int32_t *block_tables;
+    int max_blocks;
+    const int32_t *context_lens;
+    const int64_t *cu_off;
+    int n_seqs;
+    void *k_out;
+    void *v_out;
+};
+int launch_gather_kv(const GatherArgs &a, cudaStream_t stream);
+
+struct AttnArgs {
+    pf_pool *pool;
+    int layer;
+    const void *q;
+    const int32_t *block_tables;
+    int max_blocks;
+    const int32_t *context_lens;
+    int n_seqs;
+    int n_q_heads;
+    float scale;
+    void *out;
+    int out_dtype;
+    int chunk_tokens;   // tokens per work item (multiple of kTileTokens)
+    void *workspace;
+    size_t ws_bytes;
+};
+int launch_attention(const AttnArgs &a, cudaStream_t stream);
+
+// Chunk length (tokens) the attention uses for a split setting; 0 on error.
+int attention_chunk_tokens(const pf_pool *pool, int max_blocks, int split_tokens);
+// Workspace layout: counters first (256-byte aligned), then fp32 partials.
+size_t attention_counter_bytes(int n_seqs, int n_kv_heads);
+size_t attention_partial_bytes(const pf_pool *pool, int n_seqs, int n_q_heads,
+                               int max_blocks, int chunk_tokens);
+
+}  // namespace pkv

@@ -1,0 +1,184 @@
+"""Paged decode attention on the GPU against the fp64 oracle.
+
+Tolerance (the stated target): max abs err <= 2e-3 and mean abs err <= 2e-4
+against the unrounded fp64 result, fp16 inputs ~ N(0, 1)."""
+import math
+
+import numpy as np
+import pytest
+
+import synth_inputs as si
+from gpu_util import PagedCase, assert_close_to_oracle, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _tiny(pkv, cuda_dev, shuffled=True):
+    w = si.WORKLOADS["tiny"]
+    lens = si.uniform_lengths(w["n_seqs"], w["len_lo"], w["len_hi"])
+    return PagedCase(pkv, cuda_dev, lens, w["n_q_heads"], w["n_kv_heads"], w["head_dim"], w["block_size"],
+                     n_blocks=w["n_blocks"], shuffle_seed=si.SEED_SHUFFLE if shuffled else 0), w["scale"]
+
+
+@pytest.mark.parametrize("split", [0, -1, 16, 48])
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_tiny_matches_oracle(pkv, cuda_dev, oracle_mod, split, out_f32):
+    import torch
+    c, scale = _tiny(pkv, cuda_dev)
+    out = c.attention(scale, split=split, out_dtype=torch.float32 if out_f32 else torch.float16)
+    ref = c.oracle(oracle_mod, scale)
+    assert_close_to_oracle(host(out), ref, what=f"tiny split={split}")
+    if out_f32:   # fp32 output has no fp16 rounding: hold it much tighter
+        assert_close_to_oracle(host(out), ref, max_abs=1e-5, mean_abs=1e-6, what="tiny fp32")
+    assert pkv.pf_device_status(reset=True) == 0
+
+
+def test_tiny_brute_force_edge_lengths(pkv, cuda_dev, oracle_mod):
+    # every length from 1 to 70 (one to five pages, ragged tails), plus 0
+    import torch
+    lens = np.array([0] + list(range(1, 71)), dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 4, 2, 64, 16)
+    for split in (0, 16, 32, -1):
+        out = c.attention(0.125, split=split, out_dtype=torch.float32)
+        ref = c.oracle(oracle_mod, 0.125)
+        assert np.all(host(out)[0] == 0.0)
+        assert_close_to_oracle(host(out), ref, max_abs=1e-5, mean_abs=1e-6, what=f"edge split={split}")
+
+
+def test_single_token_is_exact_value(pkv, cuda_dev):
+    lens = np.ones(9, dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 12, 12, 64, 16)
+    out = host(c.attention(0.125))
+    for s in range(9):
+        blk = c.bt[s, 0]
+        assert np.array_equal(out[s].view(np.uint16), c.v_host[0, blk, 0].view(np.uint16))
+
+
+def test_tail_slots_are_never_read(pkv, cuda_dev, oracle_mod):
+    lens = np.array([1, 7, 16, 17, 30, 100], dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 12, 12, 64, 16)
+    # poison every slot a sequence does not use, including whole unused blocks
+    k, v = c.k_host.copy(), c.v_host.copy()
+    used = np.zeros((c.n_blocks, 16), dtype=bool)
+    for s, L in enumerate(lens):
+        for t in range(L):
+            used[c.bt[s, t // 16], t % 16] = True
+    k[0][~used] = np.float16(np.nan)
+    v[0][~used] = np.float16(np.nan)
+    c.k_dev.copy_(dev(k, cuda_dev))
+    c.v_dev.copy_(dev(v, cuda_dev))
+    for split in (0, 16, -1):
+        out = host(c.attention(0.125, split=split))
+        ref = oracle_mod.attention_paged(c.q, k, v, 0, c.bt, lens, 0.125)
+        assert_close_to_oracle(out, ref, what=f"poisoned tails split={split}")
+
+
+def test_mixed_full_size_shuffled_and_ordered(pkv, cuda_dev, oracle_mod):
+    """The 128-sequence mixed-length workload at full size (4096 blocks of 16),
+    in the launch configuration the benchmark times (auto split), every output
+    checked.  The same token rows are written by the library's scatter into
+    ordered and into shuffled frames; both give bit-identical results (the
+    reduction order never depends on block ids)."""
+    w = si.WORKLOADS["mixed"]
+    lens = si.band_lengths(w["bands"])
+    off = si.cu_offsets(lens)
+    T = int(off[-1])
+    kc = si.fp16_normal((T, 12, 64), 301)
+    vc = si.fp16_normal((T, 12, 64), 302)
+    q = si.fp16_normal((len(lens), 12, 64), 303)
+    ref = oracle_mod.attention_contiguous(q, kc, vc, off, lens, w["scale"])
+    seq_idx = np.repeat(np.arange(len(lens)), lens).astype(np.int32)
+    pos = np.concatenate([np.arange(L) for L in lens]).astype(np.int32)
+    outs = []
+    for shuffled in (True, False):
+        c = PagedCase(pkv, cuda_dev, lens, 12, 12, 64, 16, n_blocks=w["n_blocks"],
+                      shuffle_seed=si.SEED_SHUFFLE if shuffled else 0, max_blocks=128)
+        pkv.pf_write_kv(c.pool, 0, dev(kc, cuda_dev), dev(vc, cuda_dev), c.bt_dev,
+                        dev(seq_idx, cuda_dev), dev(pos, cuda_dev))
+        out = host(c.attention(w["scale"], split=0, q_dev=dev(q, cuda_dev)))
+        assert_close_to_oracle(out, ref, what=f"mixed shuffled={shuffled}")
+        outs.append(out)
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+
+
+@pytest.mark.parametrize("batch", [1, 4])
+def test_13b_like_split_and_no_split(pkv, cuda_dev, oracle_mod, batch):
+    w = si.WORKLOADS["13b"]
+    lens = np.full(batch, w["context_len"], dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, w["n_q_heads"], w["n_kv_heads"], w["head_dim"], w["block_size"])
+    ref = c.oracle(oracle_mod, w["scale"])
+    for split in (-1, 0, 256):
+        out = host(c.attention(w["scale"], split=split))
+        assert_close_to_oracle(out, ref, what=f"13b batch={batch} split={split}")
+
+
+def test_gqa_block_size_sweep_same_tokens(pkv, cuda_dev, oracle_mod):
+    """14 q-heads / 2 kv-heads; the same token stream stored with block sizes
+    1, 16, 64, 256 gives the oracle's result, and bit-identical outputs across
+    block sizes (tiles are 16 tokens whatever the page size)."""
+    w = si.WORKLOADS["gqa"]
+    lens = si.uniform_lengths(48, w["len_lo"], w["len_hi"])
+    Hq, Hkv, D = w["n_q_heads"], w["n_kv_heads"], w["head_dim"]
+    off = si.cu_offsets(lens)
+    T = int(off[-1])
+    kc = si.fp16_normal((T, Hkv, D), 201)
+    vc = si.fp16_normal((T, Hkv, D), 202)
+    q = si.fp16_normal((len(lens), Hq, D), 203)
+    ref = oracle_mod.attention_contiguous(q, kc, vc, off, lens, w["scale"])
+    seq_idx = np.repeat(np.arange(len(lens)), lens).astype(np.int32)
+    pos = np.concatenate([np.arange(L) for L in lens]).astype(np.int32)
+    results = []
+    for B in w["block_sizes"]:
+        c = PagedCase(pkv, cuda_dev, lens, Hq, Hkv, D, B)
+        # write the token stream through the library's own scatter
+        pkv.pf_write_kv(c.pool, 0, dev(kc, cuda_dev), dev(vc, cuda_dev), c.bt_dev,
+                        dev(seq_idx, cuda_dev), dev(pos, cuda_dev))
+        out = host(c.attention(w["scale"], q_dev=dev(q, cuda_dev)))
+        assert_close_to_oracle(out, ref, what=f"gqa B={B}")
+        results.append(out)
+    for r in results[1:]:
+        assert np.array_equal(r.view(np.uint16), results[0].view(np.uint16))
+
+
+@pytest.mark.parametrize("hq,hkv,d", [(8, 1, 64), (6, 2, 128), (5, 5, 128), (16, 2, 64), (24, 8, 128)])
+def test_head_layouts(pkv, cuda_dev, oracle_mod, hq, hkv, d):
+    lens = si.uniform_lengths(11, 1, 600, seed=9)
+    c = PagedCase(pkv, cuda_dev, lens, hq, hkv, d, 16)
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    ref = c.oracle(oracle_mod, scale)
+    for split in (0, 32):
+        assert_close_to_oracle(host(c.attention(scale, split=split)), ref, what=f"{hq}/{hkv}x{d} split={split}")
+
+
+def test_workspace_is_reusable_and_results_repeat(pkv, cuda_dev, oracle_mod):
+    lens = si.uniform_lengths(40, 1, 3000, seed=10)
+    c = PagedCase(pkv, cuda_dev, lens, 12, 12, 64, 16)
+    ws = pkv.make_workspace(c.pool, len(lens), 12, c.bt.shape[1], 64)
+    a = host(c.attention(0.125, split=64, ws=ws))
+    b = host(c.attention(0.125, split=64, ws=ws))
+    assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
+    assert_close_to_oracle(a, c.oracle(oracle_mod, 0.125), what="reuse")
+    # the per-(seq, head) counters are back at zero after each call
+    import torch
+    cnt = host(ws[: len(lens) * 12 * 4].view(torch.int32))
+    assert np.all(cnt == 0)
+
+
+def test_many_short_sequences_and_large_batch(pkv, cuda_dev, oracle_mod):
+    lens = si.uniform_lengths(3000, 0, 40, seed=11)
+    c = PagedCase(pkv, cuda_dev, lens, 4, 4, 64, 16)
+    out = host(c.attention(0.125))
+    ref = c.oracle(oracle_mod, 0.125)
+    assert np.all(out[lens == 0] == 0)
+    assert_close_to_oracle(out, ref, what="3000 short seqs")
+
+
+def test_bad_block_id_is_flagged(pkv, cuda_dev):
+    lens = np.array([40, 40], dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 12, 12, 64, 16)
+    bad = c.bt.copy()
+    bad[1, 2] = c.n_blocks + 100
+    c.bt_dev = dev(bad, cuda_dev)
+    pkv.pf_device_status(reset=True)
+    c.attention(0.125)
+    assert pkv.pf_device_status(reset=True) == pkv.PF_DEV_BAD_BLOCK_ID
