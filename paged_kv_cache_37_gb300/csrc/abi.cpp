@@ -149,10 +149,9 @@ size_t pf_decode_workspace_bytes(const pf_pool *pool, int n_seqs, int n_q_heads,
         pkv::set_error(PF_ERR_INVALID, "pf_decode_workspace_bytes: bad arguments");
         return 0;
     }
-    int chunk = pkv::attention_chunk_tokens(pool, max_blocks_per_seq, split_tokens);
-    if (chunk <= 0) return 0;
-    return pkv::attention_counter_bytes(n_seqs, pool->n_kv_heads) +
-           pkv::attention_partial_bytes(pool, n_seqs, n_q_heads, max_blocks_per_seq, chunk);
+    pkv::AttnPlan plan;
+    if (pkv::attention_plan(pool, n_seqs, n_q_heads, max_blocks_per_seq, split_tokens, false, &plan)) return 0;
+    return plan.counter_bytes + plan.partial_bytes;
 }
 
 int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
@@ -192,16 +191,23 @@ int pf_paged_decode_attention(const pf_pool *pool, int layer, const void *q,
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_decode_attention: max_blocks_per_seq must be positive");
     if (!(scale > 0.0f) || scale != scale)
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_decode_attention: scale must be a positive number");
-    int chunk = pkv::attention_chunk_tokens(pool, max_blocks_per_seq, split_tokens);
-    if (chunk <= 0) return PF_ERR_INVALID;
-    size_t need = pkv::attention_counter_bytes(n_seqs, pool->n_kv_heads) +
-                  pkv::attention_partial_bytes(pool, n_seqs, n_q_heads, max_blocks_per_seq, chunk);
+    pkv::AttnPlan plan;
+    // host-only checks first (no device query), then the device-sized plan
+    rc = pkv::attention_plan(pool, n_seqs, n_q_heads, max_blocks_per_seq, split_tokens, false, &plan);
+    if (rc) return rc;
+    if (ws_bytes < plan.counter_bytes)
+        return pkv::set_error(PF_ERR_INVALID, "pf_paged_decode_attention: workspace has " +
+                                                  std::to_string(ws_bytes) + " bytes, needs at least " +
+                                                  std::to_string(plan.counter_bytes));
+    rc = pkv::attention_plan(pool, n_seqs, n_q_heads, max_blocks_per_seq, split_tokens, true, &plan);
+    if (rc) return rc;
+    const size_t need = plan.counter_bytes + plan.partial_bytes;
     if (ws_bytes < need)
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_decode_attention: workspace has " +
                                                   std::to_string(ws_bytes) + " bytes, needs " +
                                                   std::to_string(need));
     pkv::AttnArgs a{const_cast<pf_pool *>(pool), layer, q, block_tables, max_blocks_per_seq, context_lens,
-                    n_seqs, n_q_heads, scale, out, out_dtype, chunk, workspace, ws_bytes};
+                    n_seqs, n_q_heads, scale, out, out_dtype, plan, workspace, ws_bytes};
     return pkv::launch_attention(a, static_cast<cudaStream_t>(stream));
 }
 

@@ -49,14 +49,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Suspend hint for try_wait: the hardware parks a waiting thread until the
+// phase completes or this many nanoseconds pass, so waits cost no issue slots.
+constexpr uint32_t kSuspendHintNs = 200000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
         : "memory");
     return ok != 0;
 }
@@ -68,7 +72,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *st
     unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
             atomicOr(status, PF_DEV_WAIT_TIMEOUT);
             return false;
         }
@@ -92,6 +96,15 @@ __device__ __forceinline__ bool warps_sync(uint32_t bar, uint32_t &phase, int *s
     const bool ok = warp_wait(bar, phase & 1u, status, lane);
     ++phase;
     return ok;
+}
+
+// Atomic add with acquire-release semantics at GPU scope: publishes this
+// thread's (and, by cumulativity, its CTA's synchronised) earlier writes and
+// observes those published by earlier adders.
+__device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
 }
 
 // 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.

@@ -80,6 +80,17 @@ struct GatherArgs {
 };
 int launch_gather_kv(const GatherArgs &a, cudaStream_t stream);
 
+// How an attention call is scheduled and what workspace it needs.
+struct AttnPlan {
+    bool spans;            // balanced spans (split_tokens == 0) or fixed chunks
+    int chunk;             // chunk schedule: tokens per chunk
+    int grid;              // persistent grid (0 when planned without a device)
+    size_t counter_bytes;  // per (sequence, kv-head) counters, 256-byte aligned
+    size_t partial_bytes;  // fp32 partial records
+};
+int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_blocks, int split_tokens,
+                   bool need_device, AttnPlan *plan);
+
 struct AttnArgs {
     pf_pool *pool;
     int layer;
@@ -92,17 +103,10 @@ struct AttnArgs {
     float scale;
     void *out;
     int out_dtype;
-    int chunk_tokens;   // tokens per work item (multiple of kTileTokens)
+    AttnPlan plan;
     void *workspace;
     size_t ws_bytes;
 };
 int launch_attention(const AttnArgs &a, cudaStream_t stream);
-
-// Chunk length (tokens) the attention uses for a split setting; 0 on error.
-int attention_chunk_tokens(const pf_pool *pool, int max_blocks, int split_tokens);
-// Workspace layout: counters first (256-byte aligned), then fp32 partials.
-size_t attention_counter_bytes(int n_seqs, int n_kv_heads);
-size_t attention_partial_bytes(const pf_pool *pool, int n_seqs, int n_q_heads,
-                               int max_blocks, int chunk_tokens);
 
 }  // namespace pkv
