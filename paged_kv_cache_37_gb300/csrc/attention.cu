@@ -3,6 +3,7 @@
 // persistent kernel (device code in attention_kernel.cuh).
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "attention_kernel.cuh"
@@ -112,8 +113,24 @@ int resident_grid(const pf_pool *pool, int n_q_heads, int *grid) {
     return PF_OK;
 }
 
+// Merge-job stamp of each main-kernel launch (never 0, so a zeroed
+// workspace holds no job of any launch).
+std::atomic<unsigned> g_epoch{0};
+unsigned next_epoch() {
+    unsigned e = ++g_epoch;
+    if (e == 0) e = ++g_epoch;
+    return e;
+}
+
 // Grid bound used to size span records when no device can be queried.
 constexpr int kGridBoundNoDevice = 4096;
+
+// Spans per CTA of the span schedule: more spans balance the CTAs' finishing
+// times better; each span boundary adds one partial record to merge.
+#ifndef PKV_SPANS_PER_CTA
+#define PKV_SPANS_PER_CTA 4
+#endif
+constexpr int kSpansPerCta = PKV_SPANS_PER_CTA;
 
 }  // namespace
 
@@ -138,8 +155,9 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
         rc = resident_grid(pool, n_q_heads, &plan->grid);
         if (rc) return rc;
     }
-    const size_t cnt = (size_t)n_seqs * (size_t)pool->n_kv_heads * sizeof(int);
-    plan->counter_bytes = (cnt + 255) / 256 * 256;
+    // [scheduler words: 256 B][fp32 records][merge jobs]
+    plan->counter_bytes = 256;
+    const int ng = (pool->n_kv_heads + HG - 1) / HG;
     if (plan->spans) {
         plan->chunk = TB;
         int grid = plan->grid;
@@ -147,16 +165,25 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
             clear_error();
             grid = kGridBoundNoDevice;
         }
-        // two records (first and last segment of a span) per CTA and head of the group
-        plan->partial_bytes = (size_t)grid * 2 * (size_t)HG * rec_bytes;
+        // two records (first and last segment of a span) per span and head
+        // of the group; one job slot per record slot
+        const size_t slots = (size_t)grid * kSpansPerCta * 2;
+        plan->n_jobs = slots;
+        plan->partial_bytes = slots * (size_t)HG * rec_bytes + slots * sizeof(attn::Job);
     } else {
         long long c = split_tokens == -1 ? cap : ((long long)split_tokens + TB - 1) / TB * TB;
         if (c > cap) c = cap;
         if (c < TB) c = TB;
         plan->chunk = (int)c;
         const long long per_seq = (maxctx + c - 1) / c;
-        plan->partial_bytes = per_seq <= 1 ? 0
-                                           : (size_t)per_launch * (size_t)per_seq * (size_t)pool->n_kv_heads * rec_bytes;
+        if (per_seq <= 1) {
+            plan->n_jobs = 0;   // no sequence is ever cut: nothing to merge
+            plan->partial_bytes = 0;
+        } else {
+            const size_t units = (size_t)per_launch * (size_t)per_seq;
+            plan->n_jobs = units * ng;
+            plan->partial_bytes = units * (size_t)pool->n_kv_heads * rec_bytes + plan->n_jobs * sizeof(attn::Job);
+        }
     }
     return PF_OK;
 }
@@ -178,8 +205,11 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     const AttnPlan &plan = a.plan;
 
     attn::Params p;
-    p.counters = static_cast<int *>(a.workspace);
+    p.sched = static_cast<int *>(a.workspace);
     p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + plan.counter_bytes);
+    const size_t rec_bytes = plan.partial_bytes - plan.n_jobs * sizeof(attn::Job);
+    p.jobs = reinterpret_cast<attn::Job *>(static_cast<uint8_t *>(a.workspace) + plan.counter_bytes + rec_bytes);
+    p.spans_per_cta = kSpansPerCta;
     p.status = status;
     p.max_blocks = a.max_blocks;
     p.n_q_heads = a.n_q_heads;
@@ -196,19 +226,38 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     const size_t row = (size_t)a.n_q_heads * pool->head_dim;   // q / out elements per sequence
 
     // Sequences are independent: batches larger than one launch's share of
-    // shared memory run as consecutive launches on the stream (they reuse
-    // the partial records; counters are per sequence).
+    // shared memory run as consecutive launches on the stream; each launch
+    // stamps its merge jobs with a fresh epoch.
     for (int s0 = 0; s0 < a.n_seqs; s0 += attn::kMaxSeqsPerLaunch) {
         const int n = a.n_seqs - s0 < attn::kMaxSeqsPerLaunch ? a.n_seqs - s0 : attn::kMaxSeqsPerLaunch;
         p.q = static_cast<const __half *>(a.q) + (size_t)s0 * row;
         p.out = static_cast<uint8_t *>(a.out) + (size_t)s0 * row * out_elem;
         p.bt = a.block_tables + (size_t)s0 * a.max_blocks;
         p.lens = a.context_lens + s0;
-        p.counters = static_cast<int *>(a.workspace) + (size_t)s0 * pool->n_kv_heads;
         p.n_seqs = n;
+        p.epoch = next_epoch();
         ki.fn<<<plan.grid, attn::NTHREADS, ki.smem, stream>>>(pool->tmap_k[dev], pool->tmap_v[dev], p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_error(e, "pf_paged_decode_attention: launch");
+        if (plan.n_jobs == 0) continue;
+        // merge grid: a programmatic dependent of the main grid (it launches
+        // while the main grid drains and waits for it before reading)
+        const int n_jobs = (int)plan.n_jobs;
+        unsigned long long warps = (unsigned long long)plan.n_jobs * HG;   // one per (job slot, head)
+        unsigned blocks = (unsigned)((warps + 3) / 4);
+        if (blocks > 4096) blocks = 4096;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(blocks);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = 0;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, ki.merge, p, n_jobs);
+        if (e != cudaSuccess) return cuda_error(e, "pf_paged_decode_attention: merge launch");
     }
     return PF_OK;
 }

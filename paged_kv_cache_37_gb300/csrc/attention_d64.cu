@@ -8,7 +8,7 @@ namespace {
 
 template <int G, int HG>
 KernelInfo info() {
-    return {paged_decode_kernel<64, G, HG>, sizeof(Smem<64, G, HG>)};
+    return {paged_decode_kernel<64, G, HG>, sizeof(Smem<64, G, HG>), merge_kernel<64, G, HG>};
 }
 
 template <int HG>
@@ -22,7 +22,7 @@ KernelInfo by_group(int g) {
         case 6: return info<6, HG>();
         case 7: return info<7, HG>();
         case 8: return info<8, HG>();
-        default: return {nullptr, 0};
+        default: return {nullptr, 0, nullptr};
     }
 }
 
@@ -33,7 +33,7 @@ KernelInfo kernel_d64(int g, int hg) {
         case 1: return by_group<1>(g);
         case 2: return by_group<2>(g);
         case 4: return by_group<4>(g);
-        default: return {nullptr, 0};
+        default: return {nullptr, 0, nullptr};
     }
 }
 

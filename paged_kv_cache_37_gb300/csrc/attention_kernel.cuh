@@ -38,10 +38,12 @@
 //   reference maximum is only raised when a score passes it by more than 2^8
 //   (exact up to rounding: all terms share the reference); acc += p v.
 // * End of item: token groups merge by shuffles (and the WPH warps of a head
-//   through shared memory).  A whole sequence writes `out`; a chunk writes
-//   its partial (acc[D], m, l) to the workspace, and the warp whose acq_rel
-//   counter increment completes the count for (s, h) merges the partials of
-//   that head and writes `out`, then resets the counter.  Nobody waits.
+//   through shared memory).  A whole pair writes `out`.  A part of a cut pair
+//   writes its record (acc[D], m, l per q-head) with plain stores, and the
+//   first part of the pair also writes a merge job stamped with the call's
+//   epoch.  merge_kernel, launched next on the stream as a programmatic
+//   dependent of this grid, merges the records of every job of this epoch
+//   with the log-sum-exp rule.  No CTA waits for another.
 // * Every wait is bounded (1 s) and parks the thread in hardware while it
 //   waits; a timeout sets PF_DEV_WAIT_TIMEOUT and the CTA returns after
 //   waiting (bounded) for its own copies in flight.
@@ -54,7 +56,7 @@ namespace attn {
 
 constexpr int TB = 16;                // tokens per staged tile
 constexpr int NCW = 4;                // consumer warps
-constexpr int NTHREADS = 32 * (NCW + 1);
+constexpr int NTHREADS = 32 * (NCW + 1);  // producer, consumers
 constexpr int NQ = 2;                 // item (q) slots
 constexpr float kRescaleLog2 = 8.0f;  // raise the reference max past 2^8
 constexpr unsigned FULL = 0xffffffffu;
@@ -69,11 +71,21 @@ struct ItemDesc {
     int kind;   // ItemKind
     int a;      // kChunk: global chunk index; kSpanPart: flattened first tile of the pair
     int b;      // kChunk: chunk index in the sequence; kSpanPart: tiles of the pair
-    int c;      // kChunk: chunks of the sequence; kSpanPart: this CTA's record slot (0/1)
+    int c;      // kChunk: chunks of the sequence; kSpanPart: record slot (0/1) in the span
+    int span;   // kSpanPart: span index
+    int pad0, pad1, pad2;
+};
+
+// A cut pair to merge: records first .. first + n_parts - 1 (chunk records
+// (unit * Hkv + h), or span records ((span * 2 + slot) * HG + hl) where only
+// the first span can use slot 1).
+struct Job {
+    int s, h0, kind, first, z_first, n_parts;
+    unsigned epoch;
+    int pad;
 };
 
 constexpr int kMaxSeqsPerLaunch = 1024;   // the span schedule keeps lengths in shared memory
-constexpr int kSeqSmemInts = 2 * kMaxSeqsPerLaunch + 4;
 
 struct Params {
     const __half *q;
@@ -81,7 +93,8 @@ struct Params {
     const int32_t *bt;
     const int32_t *lens;
     float *partials;
-    int *counters;
+    struct Job *jobs;
+    unsigned epoch;   // this launch's stamp for merge jobs (never 0)
     int *status;
     int n_seqs;
     int max_blocks;
@@ -93,15 +106,20 @@ struct Params {
     int layer_row0;   // layer * n_blocks * block_size (< 2^31, checked at pool creation)
     int chunk;        // chunk schedule: tokens per chunk, multiple of TB
     int spans;        // 1 = span schedule, 0 = chunk schedule
+    int spans_per_cta;// span schedule: spans = min(W, grid * spans_per_cta)
+    int *sched;       // span schedule: [0] next span ticket, [1] CTAs done (zero between calls)
     int out_f32;
     float scale_log2; // scale * log2(e)
 };
 
-// Span schedule over W flattened tiles and n = min(grid, W) CTAs (so no span
-// is empty): CTA b < n owns tiles [span_start(b), span_start(b+1)).
+// Span schedule: W flattened tiles cut into n = min(W, grid * spans_per_cta)
+// spans (none empty); span j holds tiles [span_start(j), span_start(j+1)).
 __device__ __forceinline__ long long span_start(long long b, long long W, long long n) { return b * W / n; }
-__device__ __forceinline__ long long span_ctas(long long W) { return W < (long long)gridDim.x ? W : gridDim.x; }
-// The CTA whose span holds flattened tile x.
+__device__ __forceinline__ long long span_count(long long W, int per_cta) {
+    const long long n = (long long)gridDim.x * per_cta;
+    return W < n ? W : n;
+}
+// The span that holds flattened tile x.
 __device__ __forceinline__ long long span_owner(long long x, long long W, long long n) {
     return ((x + 1) * n - 1) / W;
 }
@@ -131,16 +149,17 @@ struct __align__(128) Smem {
     uint64_t cbar;   // consumer-warps barrier (count NCW), used when WPH > 1
     int warp_tot[NTHREADS / 32];
     // span schedule: pre[s] = tiles (per group) of sequences before s, for
-    // s = 0..S; len[s] = clamped length of sequence s
+    // s = 0..S; rem[s] = tokens of sequence s in its last tile (1..16), so
+    // its clamped length is (pre[s + 1] - pre[s] - 1) * 16 + rem[s]
     int pre[kMaxSeqsPerLaunch + 1];
-    int len[kMaxSeqsPerLaunch];
+    uint8_t rem[kMaxSeqsPerLaunch];
 };
 
 // ------------------------------------------------------------ producer
 
 struct ProdItem {
     bool done;
-    int s, h0, tok0, ntok, kind, a, b, c, pg0, npg;
+    int s, h0, tok0, ntok, kind, a, b, c, span, pg0, npg;
     int ids0, ids1;   // raw block ids of pages pg0 + lane and pg0 + 32 + lane
 };
 
@@ -235,22 +254,38 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         return it;
     };
 
-    // ---- span schedule: this CTA's flattened tiles [x, xend)
+    // ---- span schedule: spans are taken in turn -- the first one is span
+    // blockIdx.x, later ones come from an atomic ticket fetched one span
+    // ahead -- and walked segment by segment.
     const int S = p.n_seqs;
-    long long W = 0, x = 0, xend = 0;
-    long long n_span = 0;
+    long long W = 0, n_span = 0, x = 0, xend = 0, span = -1;
+    int ticket = 0;   // lane 0: raw value of the ticket taken for the next span
+    // The ticket's value is only read (broadcast) when the next span starts,
+    // so the atomic's latency overlaps with this span's work.
+    auto take_ticket = [&]() {
+        if (lane == 0) ticket = atomicAdd(&p.sched[0], 1);
+    };
+    auto enter_span = [&](long long j) {
+        span = j;
+        if (j < n_span) {
+            x = span_start(j, W, n_span);
+            xend = span_start(j + 1, W, n_span);
+            take_ticket();   // for the span after this one
+        } else {
+            x = xend = 0;
+        }
+    };
     if (p.spans) {
         W = (long long)sm.pre[S] * ng;
-        n_span = span_ctas(W);
-        if (blockIdx.x < n_span) {
-            x = span_start(blockIdx.x, W, n_span);
-            xend = span_start(blockIdx.x + 1, W, n_span);
-        }
+        n_span = span_count(W, p.spans_per_cta);
+        enter_span(blockIdx.x);
+        if (span >= n_span) take_ticket();   // every CTA ends with exactly one ticket past the end
     } else {
         load_window(0);
     }
     auto decode_span = [&]() {
         ProdItem it;
+        if (x >= xend && span < n_span) enter_span((long long)gridDim.x + __shfl_sync(FULL, ticket, 0));
         it.done = x >= xend;
         if (it.done) return it;
         // largest s with pre[s] * ng <= x (it has tiles: pre[s + 1] * ng > x)
@@ -274,9 +309,10 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         it.kind = whole ? kWhole : kSpanPart;
         it.a = (int)(pair0 + (long long)grp * nt);       // flattened first tile of the pair
         it.b = nt;
-        it.c = (x == span_start(blockIdx.x, W, n_span)) ? 0 : 1;
+        it.c = (x == span_start(span, W, n_span)) ? 0 : 1;
+        it.span = (int)span;
         x += len;
-        finish_decode(it, sm.len[s]);
+        finish_decode(it, (nt - 1) * TB + sm.rem[s]);
         return it;
     };
     auto decode = [&](int k) { return p.spans ? decode_span() : decode_chunk(k); };
@@ -307,6 +343,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
             d.a = it.a;
             d.b = it.b;
             d.c = it.c;
+            d.span = it.span;
             sm.desc[slot] = d;
             const int nv = min(HG, p.n_kv_heads - it.h0);           // heads that exist
             const uint32_t qbytes = (uint32_t)nv * G * D * 2;
@@ -367,6 +404,14 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         it = nx;
     }
 
+    // Span schedule: every CTA ends with exactly one ticket past the end; the
+    // CTA that finishes last resets the scheduler words for the next call.
+    if (p.spans && lane == 0) {
+        if (atomic_add_acq_rel_gpu(&p.sched[1], 1) == (int)gridDim.x - 1) {
+            atomicExch(&p.sched[0], 0);
+            atomicExch(&p.sched[1], 0);
+        }
+    }
     // Wait (bounded) for this CTA's last copies so none is in flight when the
     // CTA retires, whatever happened above.
     const uint32_t last = st < (uint32_t)NS ? st : (uint32_t)NS;
@@ -397,46 +442,34 @@ __device__ __forceinline__ void store8(const Params &p, size_t o, const float (&
     }
 }
 
-// Finish one (item, head) from the state a warp holds: lanes 0 .. D/8 - 1
-// hold dims [8 * lane, 8 * lane + 8) of acc; m and l are the same in every
-// lane.  A whole pair writes out.  A part writes its partial record, counts
-// it, and if this warp's count completes the head, merges every record of the
-// head (chunk records, or the span records of the CTAs that share the pair).
-template <int D, int G, int HG>
-__device__ __forceinline__ void finish_head(const Params &p, const Smem<D, G, HG> &sm, const ItemDesc &d, int h,
-                                            int hl, int lane, const float (&m)[G], const float (&l)[G],
+// Normalise and store a whole pair's head from the state a warp holds:
+// lanes 0 .. D/8 - 1 hold dims [8 * lane, 8 * lane + 8) of acc.
+template <int D, int G>
+__device__ __forceinline__ void store_whole(const Params &p, const ItemDesc &d, int h, int lane, const float (&l)[G],
                                             const float (&acc)[G][8]) {
     constexpr int LPT = D / 8;
-    constexpr int REC = G * (D + 2);   // floats per record: per q-head acc[D], m, l
-    const int Hq = p.n_q_heads;
-    if (d.kind == kWhole) {
-        if (lane < LPT) {
+    if (lane < LPT) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                float x[8];
-                const float inv = 1.0f / l[g];
+        for (int g = 0; g < G; ++g) {
+            float x[8];
+            const float inv = 1.0f / l[g];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) x[i] = acc[g][i] * inv;
-                store8(p, ((size_t)d.s * Hq + (size_t)h * G + g) * D + lane * 8, x);
-            }
+            for (int i = 0; i < 8; ++i) x[i] = acc[g][i] * inv;
+            store8(p, ((size_t)d.s * p.n_q_heads + (size_t)h * G + g) * D + lane * 8, x);
         }
-        return;
     }
+}
+
+// Record of one part of a cut pair for head hl (state as in store_whole,
+// m and l the same in every lane); the first part also writes the pair's job.
+template <int D, int G, int HG>
+__device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG> &sm, const ItemDesc &d, int hl,
+                                           int lane, bool write_job, const float (&m)[G], const float (&l)[G],
+                                           const float (&acc)[G][8]) {
+    constexpr int LPT = D / 8;
+    constexpr int REC = G * (D + 2);
     const int Hkv = p.n_kv_heads;
-    // record of this part, and how to find every record of the head
-    long long W = 0, n_cta = 0;
-    int b_first = 0, n_parts;
-    size_t rec;
-    if (d.kind == kChunk) {
-        rec = (size_t)d.a * Hkv + h;
-        n_parts = d.c;
-    } else {
-        W = (long long)sm.pre[p.n_seqs] * p.n_groups;
-        n_cta = span_ctas(W);
-        b_first = (int)span_owner(d.a, W, n_cta);
-        n_parts = (int)span_owner((long long)d.a + d.b - 1, W, n_cta) - b_first + 1;
-        rec = ((size_t)blockIdx.x * 2 + d.c) * HG + hl;
-    }
+    const size_t rec = d.kind == kChunk ? (size_t)d.a * Hkv + d.h0 + hl : ((size_t)d.span * 2 + d.c) * HG + hl;
     float *part = p.partials + rec * REC;
     if (lane < LPT) {
 #pragma unroll
@@ -451,45 +484,29 @@ __device__ __forceinline__ void finish_head(const Params &p, const Smem<D, G, HG
             }
         }
     }
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) {
-        const int old = atomic_add_acq_rel_gpu(&p.counters[(size_t)d.s * Hkv + h], 1);
-        last = (old == n_parts - 1);
-    }
-    last = __shfl_sync(FULL, last, 0);
-    if (!last) return;
-    for (int e = lane; e < G * D; e += 32) {
-        const int g = e / D;
-        const int dd = e - g * D;
-        float mx = -INFINITY, ls = 0.0f, a = 0.0f;
-#pragma unroll 4
-        for (int i = 0; i < n_parts; ++i) {
-            size_t r;
-            if (d.kind == kChunk) {
-                r = (size_t)(d.a - d.b + i) * Hkv + h;
-            } else {
-                const long long b = b_first + i;
-                const int z = span_start(b, W, n_cta) >= d.a ? 0 : 1;
-                r = ((size_t)b * 2 + z) * HG + hl;
-            }
-            const float *pc = p.partials + r * REC + g * (D + 2);
-            const float mc = __ldcg(pc + D);
-            const float lc = __ldcg(pc + D + 1);
-            const float ac = __ldcg(pc + dd);
-            const float mn = fmaxf(mx, mc);
-            const float fo = (mx == -INFINITY) ? 0.0f : exp2f(mx - mn);
-            const float fc = exp2f(mc - mn);
-            ls = ls * fo + lc * fc;
-            a = a * fo + ac * fc;
-            mx = mn;
+    if (write_job && lane == 0) {
+        Job jb;
+        jb.s = d.s;
+        jb.h0 = d.h0;
+        jb.kind = d.kind;
+        jb.pad = 0;
+        size_t j;
+        if (d.kind == kChunk) {
+            jb.first = d.a;          // chunk 0 of the sequence
+            jb.z_first = 0;
+            jb.n_parts = d.c;
+            j = (size_t)d.a * p.n_groups + d.h0 / HG;
+        } else {
+            const long long W = (long long)sm.pre[p.n_seqs] * p.n_groups;
+            const long long n_span = span_count(W, p.spans_per_cta);
+            jb.first = d.span;
+            jb.z_first = d.c;
+            jb.n_parts = (int)(span_owner((long long)d.a + d.b - 1, W, n_span) - d.span + 1);
+            j = (size_t)d.span * 2 + d.c;
         }
-        const size_t o = ((size_t)d.s * Hq + (size_t)h * G + g) * D + dd;
-        const float val = a / ls;
-        if (p.out_f32) static_cast<float *>(p.out)[o] = val;
-        else static_cast<__half *>(p.out)[o] = __float2half_rn(val);
+        jb.epoch = p.epoch;
+        p.jobs[j] = jb;
     }
-    if (lane == 0) p.counters[(size_t)d.s * Hkv + h] = 0;
 }
 
 template <int D, int G, int HG>
@@ -559,55 +576,84 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
             if (active) {
                 const __half *kt = sm.k[stage];
                 const __half *vt = sm.v[stage];
+                const int tile0 = d.tok0 + j * TB;
+                const bool ragged = tile0 + TB > tend;     // only the last tile of an item
+                // phase 1: this lane group's scores for all of the warp's steps
+                // (independent chains: loads, dots and shuffles interleave)
+                uint4 kraw[STEPS];
+#pragma unroll
+                for (int step = 0; step < STEPS; ++step)
+                    kraw[step] = *reinterpret_cast<const uint4 *>(
+                        kt + ((part * TPT + step * TPW + grp) * HG + hl) * D + sub * 8);
+                float z[STEPS][G];
 #pragma unroll
                 for (int step = 0; step < STEPS; ++step) {
-                    const int tl = part * TPT + step * TPW + grp;
-                    const bool valid = d.tok0 + j * TB + tl < tend;
-                    const int row = (tl * HG + hl) * D + sub * 8;
-                    const uint4 kraw = *reinterpret_cast<const uint4 *>(kt + row);
-                    const uint4 vraw = *reinterpret_cast<const uint4 *>(vt + row);
                     float kf[8];
-                    half8_to_float(kraw, kf);
-                    float z[G];
+                    half8_to_float(kraw[step], kf);
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         float a = 0.0f;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) a = fmaf(qf[g][i], kf[i], a);
-                        z[g] = a;
+                        z[step][g] = a;
                     }
+                }
 #pragma unroll
-                    for (int o = LPT / 2; o > 0; o >>= 1) {
+                for (int o = LPT / 2; o > 0; o >>= 1) {
 #pragma unroll
-                        for (int g = 0; g < G; ++g) z[g] += __shfl_xor_sync(FULL, z[g], o);
+                    for (int step = 0; step < STEPS; ++step) {
+#pragma unroll
+                        for (int g = 0; g < G; ++g) z[step][g] += __shfl_xor_sync(FULL, z[step][g], o);
                     }
-                    bool need = false;
+                }
+                if (ragged) {
+#pragma unroll
+                    for (int step = 0; step < STEPS; ++step) {
+                        if (tile0 + part * TPT + step * TPW + grp >= tend) {
+#pragma unroll
+                            for (int g = 0; g < G; ++g) z[step][g] = -INFINITY;
+                        }
+                    }
+                }
+                // phase 2: the warp's maximum over the tile; the reference
+                // maximum m (the same in every lane) is raised only when the
+                // tile passes it by more than 2^8
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    float mt = z[0][g];
+#pragma unroll
+                    for (int step = 1; step < STEPS; ++step) mt = fmaxf(mt, z[step][g]);
+#pragma unroll
+                    for (int o = LPT; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, o));
+                    if (mt > m[g] + kRescaleLog2) {
+                        const float sc = exp2f(m[g] - mt);   // m = -inf gives 0
+                        l[g] *= sc;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[g][i] *= sc;
+                        m[g] = mt;
+                    }
+                }
+                // phase 3: weights and the weighted sum of V
+                uint4 vraw[STEPS];
+#pragma unroll
+                for (int step = 0; step < STEPS; ++step)
+                    vraw[step] = *reinterpret_cast<const uint4 *>(
+                        vt + ((part * TPT + step * TPW + grp) * HG + hl) * D + sub * 8);
+#pragma unroll
+                for (int step = 0; step < STEPS; ++step) {
+                    float vf[8];
+                    half8_to_float(vraw[step], vf);
+                    if (ragged && tile0 + part * TPT + step * TPW + grp >= tend) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) vf[i] = 0.0f;   // tail rows may hold anything
+                    }
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
-                        if (!valid) z[g] = -INFINITY;
-                        need |= z[g] > m[g] + kRescaleLog2;
-                    }
-                    if (__any_sync(FULL, need)) {
+                        // a masked score has weight 0 (also when m is still -inf)
+                        const float pz = (ragged && z[step][g] == -INFINITY) ? 0.0f : exp2f(z[step][g] - m[g]);
+                        l[g] += pz;
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float mn = fmaxf(m[g], z[g]);
-                            const float sc = (mn == -INFINITY) ? 1.0f : exp2f(m[g] - mn);
-                            l[g] *= sc;
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) acc[g][i] *= sc;
-                            m[g] = mn;
-                        }
-                    }
-                    if (valid) {
-                        float vf[8];
-                        half8_to_float(vraw, vf);
-#pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float pz = exp2f(z[g] - m[g]);
-                            l[g] += pz;
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pz, vf[i], acc[g][i]);
-                        }
+                        for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pz, vf[i], acc[g][i]);
                     }
                 }
             }
@@ -615,31 +661,20 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
             if (lane == 0) mbar_arrive(smem_addr(&sm.empty[stage]));
         }
 
-        // Merge the token groups of this warp (lanes with the same `sub`).
+        // Sum the token groups of this warp (they share the reference m).
 #pragma unroll
         for (int o = LPT; o < 32; o <<= 1) {
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const float mo = __shfl_xor_sync(FULL, m[g], o);
-                const float lo = __shfl_xor_sync(FULL, l[g], o);
-                const float mn = fmaxf(m[g], mo);
-                const float a = (m[g] == -INFINITY) ? 0.0f : exp2f(m[g] - mn);
-                const float b = (mo == -INFINITY) ? 0.0f : exp2f(mo - mn);
-                l[g] = l[g] * a + lo * b;
+                l[g] += __shfl_xor_sync(FULL, l[g], o);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const float ao = __shfl_xor_sync(FULL, acc[g][i], o);
-                    acc[g][i] = acc[g][i] * a + ao * b;
-                }
-                m[g] = mn;
+                for (int i = 0; i < 8; ++i) acc[g][i] += __shfl_xor_sync(FULL, acc[g][i], o);
             }
         }
 
-        if constexpr (WPH == 1) {
-            if (active) finish_head<D, G, HG>(p, sm, d, h, hl, lane, m, l, acc);
-        } else {
+        if constexpr (WPH > 1) {
             // The WPH warps of a head meet in shared memory; the first of
-            // them finishes the head.
+            // them carries the merged state on.
             if (lane < LPT) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
@@ -652,25 +687,24 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 }
             }
             if (!warps_sync(cbar, cphase, p.status, lane)) return;
-            if (part == 0 && active) {
-                const int w0 = cw;
+            if (part == 0) {
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     float mx = -INFINITY;
 #pragma unroll
-                    for (int w = 0; w < WPH; ++w) mx = fmaxf(mx, sm.red[w0 + w][g][D]);
+                    for (int w = 0; w < WPH; ++w) mx = fmaxf(mx, sm.red[cw + w][g][D]);
                     float ls = 0.0f;
                     float a[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) a[i] = 0.0f;
 #pragma unroll
                     for (int w = 0; w < WPH; ++w) {
-                        const float mw = sm.red[w0 + w][g][D];
+                        const float mw = sm.red[cw + w][g][D];
                         const float f = (mw == -INFINITY) ? 0.0f : exp2f(mw - mx);
-                        ls = fmaf(sm.red[w0 + w][g][D + 1], f, ls);
+                        ls = fmaf(sm.red[cw + w][g][D + 1], f, ls);
                         if (lane < LPT) {
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) a[i] = fmaf(sm.red[w0 + w][g][lane * 8 + i], f, a[i]);
+                            for (int i = 0; i < 8; ++i) a[i] = fmaf(sm.red[cw + w][g][lane * 8 + i], f, a[i]);
                         }
                     }
                     m[g] = mx;
@@ -678,15 +712,23 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
 #pragma unroll
                     for (int i = 0; i < 8; ++i) acc[g][i] = a[i];
                 }
-                finish_head<D, G, HG>(p, sm, d, h, hl, lane, m, l, acc);
             }
             if (!warps_sync(cbar, cphase, p.status, lane)) return;   // red[] is reused next item
+        }
+        const bool leader = part == 0 && active;
+        if (d.kind == kWhole) {
+            if (leader) store_whole<D, G>(p, d, h, lane, l, acc);
+        } else if (leader) {
+            // the first part of a cut pair (chunk 0, or the segment that
+            // starts at the pair's first tile) also writes the merge job
+            const bool first = d.kind == kChunk ? d.b == 0 : d.tok0 == 0;
+            write_part<D, G, HG>(p, sm, d, hl, lane, first && hl == 0, m, l, acc);
         }
     }
 }
 
 template <int D, int G, int HG>
-__global__ void __launch_bounds__(NTHREADS) paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
+__global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                  const __grid_constant__ CUtensorMap tmv,
                                                                  const Params p) {
     constexpr int NS = Shape<D, HG>::NS;
@@ -694,6 +736,9 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_kernel(const __grid_con
     Smem<D, G, HG> &sm = *reinterpret_cast<Smem<D, G, HG> *>(smem_raw);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
+    // The merge grid that follows may start launching now; it waits for
+    // this grid's completion before it reads anything.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_addr(&sm.full[i]), 1);
@@ -718,7 +763,7 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_kernel(const __grid_con
                 atomicOr(p.status, PF_DEV_BAD_LENGTH);
                 L = L < 0 ? 0 : maxctx;
             }
-            sm.len[s] = L;
+            sm.rem[s] = (uint8_t)(L - (L - 1) / TB * TB);   // unused when L = 0
             sm.pre[s + 1] = (L + TB - 1) / TB;
         }
         __syncthreads();
@@ -748,11 +793,101 @@ __global__ void __launch_bounds__(NTHREADS) paged_decode_kernel(const __grid_con
     else consumers<D, G, HG>(p, sm, warp - 1, lane);
 }
 
+// Merge the records of every job of this launch's epoch: one warp per (job
+// slot, head).  Each lane loads one part's (m, l) and, in the same round
+// trip, every part's acc values of its own dims, so a head costs about two
+// dependent memory round trips (the job, then its records).
+template <int D, int G, int HG>
+__global__ void __launch_bounds__(128, 1) merge_kernel(const Params p, int n_jobs) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the main grid has finished
+    constexpr int REC = G * (D + 2);
+    constexpr int DPL = D / 32;   // dims per lane
+    constexpr int PB = 8;         // parts whose acc loads are in flight together
+    const int lane = threadIdx.x % 32;
+    const int Hkv = p.n_kv_heads;
+    const int Hq = p.n_q_heads;
+    const long long n_warps = (long long)gridDim.x * blockDim.x / 32;
+    for (long long wi = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32; wi < (long long)n_jobs * HG;
+         wi += n_warps) {
+        const int j = (int)(wi / HG);
+        const int hl = (int)(wi - (long long)j * HG);
+        const Job jb = p.jobs[j];
+        if (jb.epoch != p.epoch || jb.h0 + hl >= Hkv) continue;
+        const int h = jb.h0 + hl;
+        const int n = jb.n_parts;
+        auto rec_of = [&](int i) -> size_t {
+            return jb.kind == kChunk ? (size_t)(jb.first + i) * Hkv + h
+                                     : ((size_t)(jb.first + i) * 2 + (i == 0 ? jb.z_first : 0)) * HG + hl;
+        };
+#pragma unroll 1
+        for (int g = 0; g < G; ++g) {
+            float mx = -INFINITY, ls = 0.0f;
+            float a[DPL];
+#pragma unroll
+            for (int q = 0; q < DPL; ++q) a[q] = 0.0f;
+            for (int i0 = 0; i0 < n; i0 += 32) {
+                const int i = i0 + lane;
+                float mi = -INFINITY, li = 0.0f;
+                if (i < n) {
+                    const float *pc = p.partials + rec_of(i) * REC + g * (D + 2);
+                    mi = __ldcg(pc + D);
+                    li = __ldcg(pc + D + 1);
+                }
+                const int nb = min(32, n - i0);
+                for (int j0 = 0; j0 < nb; j0 += PB) {
+                    float v[PB][DPL];
+#pragma unroll
+                    for (int jj = 0; jj < PB; ++jj) {
+                        if (j0 + jj < nb) {
+                            const float *pc = p.partials + rec_of(i0 + j0 + jj) * REC + g * (D + 2);
+#pragma unroll
+                            for (int q = 0; q < DPL; ++q) v[jj][q] = __ldcg(pc + lane + 32 * q);
+                        }
+                    }
+                    // running reference over the batches of 32 parts
+                    float bm = mi;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o));
+                    const float mn = fmaxf(mx, bm);
+                    if (mn > mx) {
+                        const float sc = (mx == -INFINITY) ? 0.0f : exp2f(mx - mn);
+                        ls *= sc;
+#pragma unroll
+                        for (int q = 0; q < DPL; ++q) a[q] *= sc;
+                        mx = mn;
+                    }
+                    const float w = (i < n && j0 == 0) ? exp2f(mi - mx) : 0.0f;
+                    if (j0 == 0) ls = fmaf(w, li, ls);
+#pragma unroll
+                    for (int jj = 0; jj < PB; ++jj) {
+                        const float wj = __shfl_sync(FULL, exp2f(mi - mx), j0 + jj);
+                        if (j0 + jj < nb) {
+#pragma unroll
+                            for (int q = 0; q < DPL; ++q) a[q] = fmaf(wj, v[jj][q], a[q]);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
+            const float inv = 1.0f / ls;
+#pragma unroll
+            for (int q = 0; q < DPL; ++q) {
+                const size_t o = ((size_t)jb.s * Hq + (size_t)h * G + g) * D + lane + 32 * q;
+                if (p.out_f32) static_cast<float *>(p.out)[o] = a[q] * inv;
+                else static_cast<__half *>(p.out)[o] = __float2half_rn(a[q] * inv);
+            }
+        }
+    }
+}
+
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, Params);
+using MergeFn = void (*)(Params, int);
 
 struct KernelInfo {
     KernelFn fn;
     size_t smem;
+    MergeFn merge;
 };
 
 // Defined in attention_d64.cu / attention_d128.cu.

@@ -85,8 +85,9 @@ struct AttnPlan {
     bool spans;            // balanced spans (split_tokens == 0) or fixed chunks
     int chunk;             // chunk schedule: tokens per chunk
     int grid;              // persistent grid (0 when planned without a device)
-    size_t counter_bytes;  // per (sequence, kv-head) counters, 256-byte aligned
-    size_t partial_bytes;  // fp32 partial records
+    size_t counter_bytes;  // scheduler words at the front of the workspace (256 B)
+    size_t partial_bytes;  // fp32 partial records, then merge jobs
+    size_t n_jobs;         // merge job slots (0: nothing is ever merged)
 };
 int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_blocks, int split_tokens,
                    bool need_device, AttnPlan *plan);

@@ -158,10 +158,15 @@ def test_workspace_is_reusable_and_results_repeat(pkv, cuda_dev, oracle_mod):
     b = host(c.attention(0.125, split=64, ws=ws))
     assert np.array_equal(a.view(np.uint16), b.view(np.uint16))
     assert_close_to_oracle(a, c.oracle(oracle_mod, 0.125), what="reuse")
-    # the per-(seq, head) counters are back at zero after each call
+    # the scheduler words at the front of the workspace are back at zero
     import torch
-    cnt = host(ws[: len(lens) * 12 * 4].view(torch.int32))
-    assert np.all(cnt == 0)
+    assert np.all(host(ws[:256].view(torch.int32)) == 0)
+    for split in (0, -1, 16):   # every schedule leaves them at zero
+        ws2 = pkv.make_workspace(c.pool, len(lens), 12, c.bt.shape[1], split)
+        a2 = host(c.attention(0.125, split=split, ws=ws2))
+        b2 = host(c.attention(0.125, split=split, ws=ws2))
+        assert np.array_equal(a2.view(np.uint16), b2.view(np.uint16))
+        assert np.all(host(ws2[:256].view(torch.int32)) == 0)
 
 
 def test_many_short_sequences_and_large_batch(pkv, cuda_dev, oracle_mod):
