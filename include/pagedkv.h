@@ -195,6 +195,35 @@ PF_API int pf_paged_decode_attention(const pf_pool *pool, int layer, const void 
                               int out_dtype, int split_tokens,
                               void *workspace, size_t ws_bytes, void *stream);
 
+/* The decode attention call for callers that cannot allocate device memory.
+ * No counterpart on the pages: it exists for code that may only touch the
+ * buffers it is handed -- for instance an operator inside another runtime
+ * or framework that owns every allocation -- and so cannot call cudaMalloc
+ * or any allocating routine to provide the workspace that
+ * pf_paged_decode_attention needs.  Same arguments and results as that call,
+ * without workspace / ws_bytes: the scratch is a fixed 8 MiB array inside
+ * the library (held by every GPU that loads the library until the process
+ * exits).  Nothing is allocated.
+ * - A batch whose scratch need (pf_decode_workspace_bytes) exceeds 8 MiB is
+ *   rejected with PF_ERR_INVALID; split the batch or pass a workspace to
+ *   pf_paged_decode_attention.
+ * - The first call on a device looks up the array's device address (once
+ *   per device, with that device current); make that first call before any
+ *   stream capture.
+ * - Every call on a device uses the same array and leaves its contents
+ *   behind; each call clears what must start at zero on `stream`.  Calls
+ *   that overlap on the GPU (other streams, other threads) race on the
+ *   scratch: order them on one stream. */
+PF_API int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
+                                             const void *q,
+                                             const int32_t *block_tables,
+                                             int max_blocks_per_seq,
+                                             const int32_t *context_lens,
+                                             int n_seqs, int n_q_heads,
+                                             float scale, void *out,
+                                             int out_dtype, int split_tokens,
+                                             void *stream);
+
 /* Read the device status word (OR of pf_device_flag bits set by kernels of
  * this library on the current device since the last reset) into *status_out.
  * Synchronises `stream`.  reset != 0 clears the word afterwards. */

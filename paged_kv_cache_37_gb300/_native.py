@@ -80,6 +80,7 @@ def lib():
         "pf_decode_workspace_init": (I, [P, Z, P]),
         "pf_paged_decode_attention": (I, [P, I, P, P, I, P, I, I, F, P, I, I, P, Z, P]),
         "pf_device_status": (I, [ctypes.POINTER(I), I, P]),
+        "pf_paged_decode_attention_noalloc": (I, [P, I, P, P, I, P, I, I, F, P, I, I, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -285,6 +286,25 @@ def pf_paged_decode_attention(pool, layer, q, block_tables, context_lens, scale,
         block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32), n, hq, float(scale),
         _dev_ptr(out, "out"), out_dtype, split_tokens, _dev_ptr(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+
+
+def pf_paged_decode_attention_noalloc(pool, layer, q, block_tables, context_lens, scale, out, split_tokens,
+                                      stream=None):
+    """pf_paged_decode_attention without a workspace argument: the scratch is
+    a fixed array inside the library, for callers that cannot allocate."""
+    import torch
+    n, hq, d = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.numel() != n:
+        raise PagedKVError(PF_ERR_INVALID, "block_tables must be [n_seqs, max_blocks]; context_lens [n_seqs]")
+    if tuple(out.shape) != (n, hq, d):
+        raise PagedKVError(PF_ERR_INVALID, "out must have the shape of q")
+    out_dtype = {torch.float16: PF_F16, torch.float32: PF_F32}.get(out.dtype)
+    if out_dtype is None:
+        raise PagedKVError(PF_ERR_INVALID, "out must be float16 or float32")
+    _check(lib().pf_paged_decode_attention_noalloc(
+        pool.handle, layer, _dev_ptr(q, "q", torch.float16), _dev_ptr(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32), n, hq, float(scale),
+        _dev_ptr(out, "out"), out_dtype, split_tokens, _stream_ptr(stream)))
 
 
 def pf_device_status(reset=False, stream=None):
