@@ -143,19 +143,27 @@ def profile_traffic():
     """dram bytes per attention launch from the committed ncu summary, or None
     if the kernel source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "attention_mixed_shuffled.md")
-    src = os.path.join(ROOT, "paged_kv_cache_37_gb300", "csrc", "attention.cu")
     try:
-        want = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         fields = {}
         for line in open(path):
             if ":" in line and line.startswith("- "):
                 k, v = line[2:].split(":", 1)
                 fields[k.strip()] = v.strip().strip("`")
-        if fields.get("attention.cu sha256[:16]") != want:
+        if fields.get("kernel sources sha256[:16]") != kernel_sources_hash():
             return None
-        return int(fields["dram bytes per launch"])
+        return int(fields["dram bytes per call"])
     except Exception:
         return None
+
+
+def kernel_sources_hash():
+    """Hash of the attention kernel's sources (the profile is only valid for them)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_cache_37_gb300", "csrc")
+    for name in ("attention_kernel.cuh", "attention.cu", "attention_d64.cu", "device_common.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 # --------------------------------------------------------------- clocks
@@ -337,6 +345,9 @@ def run_ours(args, dist):
                    "attn_ms": statistics.mean(b.elapsed_time(c) for _, b, c in evs)}
         return total_ms, per
 
+    # kernels per attention call: the main grid, plus the merge grid unless
+    # sequences are never split (one launch of each per 1024 sequences)
+    attn_launches = (1 if args.split == -1 else 2) * -(-S // 1024)
     a_bytes = attention_bytes(lens, Hq, Hkv, D, B)
     w_bytes = write_bytes(S, Hkv, D)
     step_bytes = a_bytes + w_bytes
@@ -474,10 +485,11 @@ def run_ours(args, dist):
                    "bytes": g_bytes, "frac_of_measured_copy": round(g_bytes / (gather_ms / 1e3) / 1e9 / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profile_traffic(),
-                     "kernel": "paged_decode_kernel<64,1>", "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                     "kernel": "pf_paged_decode_attention (paged_decode_kernel<64,1,4> + merge_kernel)",
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
         "e2e": e2e,
-        "gpu_launches": 2 * K,
+        "gpu_launches": K * (1 + attn_launches),
         "clocks": clocks,
     }
     if dist.rank == 0:

@@ -167,9 +167,10 @@ PF_API size_t pf_decode_workspace_bytes(const pf_pool *pool, int n_seqs,
                                  int n_q_heads, int max_blocks_per_seq,
                                  int split_tokens);
 
-/* Prepare a workspace for first use (zero its counters).  Needed once after
- * the workspace is allocated, and again after a call whose device status
- * reported PF_DEV_WAIT_TIMEOUT.  Successful attention calls leave it ready. */
+/* Prepare a workspace for first use (zero it).  Needed once after the
+ * workspace is allocated: merge jobs in the workspace are recognised by a
+ * per-call stamp, and zeroed memory holds no stamp of any call.  Calls leave
+ * the workspace ready for the next call. */
 PF_API int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 
 /* Single-query decode attention through the block tables (PagedAttention
@@ -211,7 +212,7 @@ PF_API int pf_paged_decode_attention(const pf_pool *pool, int layer, const void 
  *   per device, with that device current); make that first call before any
  *   stream capture.
  * - Every call on a device uses the same array and leaves its contents
- *   behind; each call clears what must start at zero on `stream`.  Calls
+ *   behind (nothing in it has to start at zero for the next call).  Calls
  *   that overlap on the GPU (other streams, other threads) race on the
  *   scratch: order them on one stream. */
 PF_API int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,

@@ -125,12 +125,7 @@ unsigned next_epoch() {
 // Grid bound used to size span records when no device can be queried.
 constexpr int kGridBoundNoDevice = 4096;
 
-// Spans per CTA of the span schedule: more spans balance the CTAs' finishing
-// times better; each span boundary adds one partial record to merge.
-#ifndef PKV_SPANS_PER_CTA
-#define PKV_SPANS_PER_CTA 4
-#endif
-constexpr int kSpansPerCta = PKV_SPANS_PER_CTA;
+
 
 }  // namespace
 
@@ -155,7 +150,7 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
         rc = resident_grid(pool, n_q_heads, &plan->grid);
         if (rc) return rc;
     }
-    // [scheduler words: 256 B][fp32 records][merge jobs]
+    // [reserved: 256 B][fp32 records][merge jobs]
     plan->counter_bytes = 256;
     const int ng = (pool->n_kv_heads + HG - 1) / HG;
     if (plan->spans) {
@@ -166,10 +161,10 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
             grid = kGridBoundNoDevice;
         }
         // two records (first and last segment of a span) per span and head
-        // of the group; one job slot per record slot
-        const size_t slots = (size_t)grid * kSpansPerCta * 2;
-        plan->n_jobs = slots;
-        plan->partial_bytes = slots * (size_t)HG * rec_bytes + slots * sizeof(attn::Job);
+        // of the group; one job slot per span
+        const size_t spans = (size_t)grid;
+        plan->n_jobs = spans;
+        plan->partial_bytes = spans * 2 * (size_t)HG * rec_bytes + spans * sizeof(attn::Job);
     } else {
         long long c = split_tokens == -1 ? cap : ((long long)split_tokens + TB - 1) / TB * TB;
         if (c > cap) c = cap;
@@ -205,11 +200,9 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     const AttnPlan &plan = a.plan;
 
     attn::Params p;
-    p.sched = static_cast<int *>(a.workspace);
     p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + plan.counter_bytes);
     const size_t rec_bytes = plan.partial_bytes - plan.n_jobs * sizeof(attn::Job);
     p.jobs = reinterpret_cast<attn::Job *>(static_cast<uint8_t *>(a.workspace) + plan.counter_bytes + rec_bytes);
-    p.spans_per_cta = kSpansPerCta;
     p.status = status;
     p.max_blocks = a.max_blocks;
     p.n_q_heads = a.n_q_heads;
@@ -243,9 +236,11 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
         // merge grid: a programmatic dependent of the main grid (it launches
         // while the main grid drains and waits for it before reading)
         const int n_jobs = (int)plan.n_jobs;
-        unsigned long long warps = (unsigned long long)plan.n_jobs * HG;   // one per (job slot, head)
+        // one warp per (job slot, head), at most one resident wave of CTAs
+        unsigned long long warps = (unsigned long long)plan.n_jobs * HG;
         unsigned blocks = (unsigned)((warps + 3) / 4);
-        if (blocks > 4096) blocks = 4096;
+        const unsigned wave = (unsigned)plan.grid * 4u;
+        if (blocks > wave) blocks = wave;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(blocks);
         cfg.blockDim = dim3(128);

@@ -106,23 +106,26 @@ struct Params {
     int layer_row0;   // layer * n_blocks * block_size (< 2^31, checked at pool creation)
     int chunk;        // chunk schedule: tokens per chunk, multiple of TB
     int spans;        // 1 = span schedule, 0 = chunk schedule
-    int spans_per_cta;// span schedule: spans = min(W, grid * spans_per_cta)
-    int *sched;       // span schedule: [0] next span ticket, [1] CTAs done (zero between calls)
+
     int out_f32;
     float scale_log2; // scale * log2(e)
 };
 
-// Span schedule: W flattened tiles cut into n = min(W, grid * spans_per_cta)
-// spans (none empty); span j holds tiles [span_start(j), span_start(j+1)).
-__device__ __forceinline__ long long span_start(long long b, long long W, long long n) { return b * W / n; }
-__device__ __forceinline__ long long span_count(long long W, int per_cta) {
-    const long long n = (long long)gridDim.x * per_cta;
-    return W < n ? W : n;
-}
-// The span that holds flattened tile x.
-__device__ __forceinline__ long long span_owner(long long x, long long W, long long n) {
-    return ((x + 1) * n - 1) / W;
-}
+// Span map of the span schedule: the W flattened tiles cut into
+// n = min(W, grid) equal spans (none empty); CTA b takes span b.  Measured on
+// the 128-sequence mixed workload, one static span per CTA beat every
+// dynamic scheme tried (ticketed spans of equal or decreasing size): small
+// spans pay per-segment costs and cut more pairs, and the merges of the cut
+// pairs cost more than the balance gains.
+struct SpanMap {
+    long long W;   // tiles in all
+    long long n;   // spans
+    __device__ __forceinline__ SpanMap(long long W_, int grid) : W(W_), n(W_ < grid ? W_ : grid) {}
+    // first tile of span j (W for j = n)
+    __device__ __forceinline__ long long start(long long j) const { return j >= n ? W : W * j / n; }
+    // the span that holds tile x
+    __device__ __forceinline__ long long owner(long long x) const { return ((x + 1) * n - 1) / W; }
+};
 
 template <int D, int HG>
 struct Shape {
@@ -254,38 +257,19 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         return it;
     };
 
-    // ---- span schedule: spans are taken in turn -- the first one is span
-    // blockIdx.x, later ones come from an atomic ticket fetched one span
-    // ahead -- and walked segment by segment.
+    // ---- span schedule: this CTA's span, walked segment by segment
     const int S = p.n_seqs;
-    long long W = 0, n_span = 0, x = 0, xend = 0, span = -1;
-    int ticket = 0;   // lane 0: raw value of the ticket taken for the next span
-    // The ticket's value is only read (broadcast) when the next span starts,
-    // so the atomic's latency overlaps with this span's work.
-    auto take_ticket = [&]() {
-        if (lane == 0) ticket = atomicAdd(&p.sched[0], 1);
-    };
-    auto enter_span = [&](long long j) {
-        span = j;
-        if (j < n_span) {
-            x = span_start(j, W, n_span);
-            xend = span_start(j + 1, W, n_span);
-            take_ticket();   // for the span after this one
-        } else {
-            x = xend = 0;
-        }
-    };
+    const SpanMap map(p.spans ? (long long)sm.pre[S] * ng : 0, gridDim.x);
+    const long long span = blockIdx.x;
+    long long x = 0, xend = 0;
     if (p.spans) {
-        W = (long long)sm.pre[S] * ng;
-        n_span = span_count(W, p.spans_per_cta);
-        enter_span(blockIdx.x);
-        if (span >= n_span) take_ticket();   // every CTA ends with exactly one ticket past the end
+        x = map.start(span);
+        xend = map.start(span + 1);
     } else {
         load_window(0);
     }
     auto decode_span = [&]() {
         ProdItem it;
-        if (x >= xend && span < n_span) enter_span((long long)gridDim.x + __shfl_sync(FULL, ticket, 0));
         it.done = x >= xend;
         if (it.done) return it;
         // largest s with pre[s] * ng <= x (it has tiles: pre[s + 1] * ng > x)
@@ -309,7 +293,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         it.kind = whole ? kWhole : kSpanPart;
         it.a = (int)(pair0 + (long long)grp * nt);       // flattened first tile of the pair
         it.b = nt;
-        it.c = (x == span_start(span, W, n_span)) ? 0 : 1;
+        it.c = (x == map.start(span)) ? 0 : 1;
         it.span = (int)span;
         x += len;
         finish_decode(it, (nt - 1) * TB + sm.rem[s]);
@@ -404,14 +388,6 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         it = nx;
     }
 
-    // Span schedule: every CTA ends with exactly one ticket past the end; the
-    // CTA that finishes last resets the scheduler words for the next call.
-    if (p.spans && lane == 0) {
-        if (atomic_add_acq_rel_gpu(&p.sched[1], 1) == (int)gridDim.x - 1) {
-            atomicExch(&p.sched[0], 0);
-            atomicExch(&p.sched[1], 0);
-        }
-    }
     // Wait (bounded) for this CTA's last copies so none is in flight when the
     // CTA retires, whatever happened above.
     const uint32_t last = st < (uint32_t)NS ? st : (uint32_t)NS;
@@ -497,12 +473,11 @@ __device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG>
             jb.n_parts = d.c;
             j = (size_t)d.a * p.n_groups + d.h0 / HG;
         } else {
-            const long long W = (long long)sm.pre[p.n_seqs] * p.n_groups;
-            const long long n_span = span_count(W, p.spans_per_cta);
+            const SpanMap map((long long)sm.pre[p.n_seqs] * p.n_groups, gridDim.x);
             jb.first = d.span;
             jb.z_first = d.c;
-            jb.n_parts = (int)(span_owner((long long)d.a + d.b - 1, W, n_span) - d.span + 1);
-            j = (size_t)d.span * 2 + d.c;
+            jb.n_parts = (int)(map.owner((long long)d.a + d.b - 1) - d.span + 1);
+            j = (size_t)d.span;   // a span is the first part of at most one cut pair
         }
         jb.epoch = p.epoch;
         p.jobs[j] = jb;

@@ -15,7 +15,7 @@
 namespace pkv {
 namespace {
 
-// Scratch of the no-allocation variant: scheduler words, partial records and
+// Scratch of the no-allocation variant: reserved bytes, partial records and
 // merge jobs of one call (the same layout as a caller's workspace).
 constexpr size_t kNoAllocScratchBytes = 8u << 20;   // 8 MiB per device
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
@@ -64,12 +64,10 @@ extern "C" int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
     void *ws = nullptr;
     int rc = pkv::scratch_for_current_device(&ws);
     if (rc) return rc;
-    // The scheduler words at the front must be zero when a call starts (a
-    // completed call leaves them zero; clearing them also recovers from a
-    // call that timed out).  Partial records and merge jobs need no clearing:
-    // every job is stamped with its own call's epoch.
-    cudaError_t e = cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return pkv::cuda_error(e, "pf_paged_decode_attention_noalloc: clearing the scratch");
+    // Nothing in the scratch has to start at zero for a call: partial records
+    // are written before they are read, and every merge job carries its own
+    // launch's epoch (the array itself is zero when the library loads, so it
+    // holds no job of any epoch at first).
     return pf_paged_decode_attention(pool, layer, q, block_tables, max_blocks_per_seq, context_lens, n_seqs,
                                      n_q_heads, scale, out, out_dtype, split_tokens, ws, pkv::kNoAllocScratchBytes,
                                      stream);

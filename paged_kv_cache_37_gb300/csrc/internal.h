@@ -85,7 +85,7 @@ struct AttnPlan {
     bool spans;            // balanced spans (split_tokens == 0) or fixed chunks
     int chunk;             // chunk schedule: tokens per chunk
     int grid;              // persistent grid (0 when planned without a device)
-    size_t counter_bytes;  // scheduler words at the front of the workspace (256 B)
+    size_t counter_bytes;  // reserved bytes at the front of the workspace (256 B)
     size_t partial_bytes;  // fp32 partial records, then merge jobs
     size_t n_jobs;         // merge job slots (0: nothing is ever merged)
 };
