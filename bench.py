@@ -4,8 +4,9 @@
 One step = one decode step of one layer over the 128-sequence mixed-length
 workload (64 x U[32,128], 38 x U[256,512], 26 x U[1024,2048] tokens; 12 heads
 x 64, fp16; a pool of 4096 blocks of 16; shuffled frames): the scatter of each
-sequence's new K/V token into its page slot (pf_write_kv), then paged decode
-attention over the grown contexts (pf_paged_decode_attention).  Inputs are
+sequence's new K/V token into its page slot and paged decode attention over
+the grown contexts, as one fused call (pf_decode_step).  The same step as two
+calls (pf_write_kv, then pf_paged_decode_attention) is timed too.  Inputs are
 resident in HBM; the step rotates over pool replicas whose total size is over
 three times the L2, so no step finds its pages in L2.
 
@@ -307,26 +308,32 @@ def run_ours(args, dist):
         wr = [(r["pool"].handle, 0, P(r["kn"]), P(r["vn"]), P(bt), S, maxb, P(seq_d), P(pos_d), S, sp) for r in reps]
         at = [(r["pool"].handle, 0, P(r["q"]), P(bt), maxb, P(lens_d), S, Hq, ctypes.c_float(w["scale"]),
                P(r["out"]), pkv.PF_F16, args.split, ws_[i][0], ws_[i][1], sp) for i, r in enumerate(reps)]
-        return wr, at
+        fu = [(r["pool"].handle, 0, P(r["q"]), P(r["kn"]), P(r["vn"]), P(bt), maxb, P(lens_d), S, Hq,
+               ctypes.c_float(w["scale"]), P(r["out"]), pkv.PF_F16, args.split, ws_[i][0], ws_[i][1], sp)
+              for i, r in enumerate(reps)]
+        return wr, at, fu
 
     def check(rc):
         if rc:
             raise pkv.PagedKVError(rc, pkv.pf_last_error())
 
-    def run_steps(layout, n, events=None):
-        wr, at = arg_sets(layout)
+    def run_steps(layout, n, events=None, fused=True):
+        wr, at, fu = arg_sets(layout)
         for i in range(n):
             r = i % R
             if events is not None:
                 events[i][0].record(stream)
-            check(lib.pf_write_kv(*wr[r]))
-            if events is not None:
-                events[i][1].record(stream)
-            check(lib.pf_paged_decode_attention(*at[r]))
+            if fused:
+                check(lib.pf_decode_step(*fu[r]))
+            else:
+                check(lib.pf_write_kv(*wr[r]))
+                if events is not None:
+                    events[i][1].record(stream)
+                check(lib.pf_paged_decode_attention(*at[r]))
             if events is not None:
                 events[i][2].record(stream)
 
-    def timed(layout, n, with_events=False):
+    def timed(layout, n, with_events=False, fused=True):
         evs = None
         if with_events:
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
@@ -334,19 +341,22 @@ def run_ours(args, dist):
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        run_steps(layout, n, evs)
+        run_steps(layout, n, evs, fused)
         e1.record(stream)
         torch.cuda.synchronize(device)
         dist.barrier()
         total_ms = e0.elapsed_time(e1)
         per = None
         if evs:
-            per = {"write_ms": statistics.mean(a.elapsed_time(b) for a, b, _ in evs),
-                   "attn_ms": statistics.mean(b.elapsed_time(c) for _, b, c in evs)}
+            if fused:
+                per = {"step_ms": statistics.mean(a.elapsed_time(c) for a, _, c in evs)}
+            else:
+                per = {"write_ms": statistics.mean(a.elapsed_time(b) for a, b, _ in evs),
+                       "attn_ms": statistics.mean(b.elapsed_time(c) for _, b, c in evs)}
         return total_ms, per
 
-    # kernels per attention call: the main grid, plus the merge grid unless
-    # sequences are never split (one launch of each per 1024 sequences)
+    # kernels per step: the fused grid, plus the merge grid unless sequences
+    # are never split (one launch of each per 1024 sequences)
     attn_launches = (1 if args.split == -1 else 2) * -(-S // 1024)
     a_bytes = attention_bytes(lens, Hq, Hkv, D, B)
     w_bytes = write_bytes(S, Hkv, D)
@@ -365,22 +375,27 @@ def run_ours(args, dist):
     time.sleep(0.2)
 
     # warm-up (also encodes the TMA descriptors and sizes the grid)
-    run_steps("shuffled", W)
-    run_steps("ordered", W)
+    for fused in (True, False):
+        run_steps("shuffled", W, fused=fused)
+        run_steps("ordered", W, fused=fused)
     torch.cuda.synchronize(device)
     pkv.pf_device_status(reset=True)
 
-    # the contract's timed region: K steps, shuffled frames
+    # the contract's timed region: K fused steps, shuffled frames
     ms_main, _ = timed("shuffled", K)
     ms_main = dist.max(ms_main)
-    # the same steps with CUDA events around every kernel (roofline, per-kernel time)
+    # the same steps with CUDA events around every call (roofline)
     ms_ev, per = timed("shuffled", K, with_events=True)
-    attn_ms = dist.max(per["attn_ms"])
-    write_ms = dist.max(per["write_ms"])
+    step_call_ms = dist.max(per["step_ms"])
     # ordered frames
     ms_ord, per_ord = timed("ordered", K, with_events=True)
     ms_ord = dist.max(ms_ord)
-    attn_ord_ms = dist.max(per_ord["attn_ms"])
+    step_ord_ms = dist.max(per_ord["step_ms"])
+    # the unfused step: pf_write_kv, then pf_paged_decode_attention
+    ms_unf, per_unf = timed("shuffled", K, with_events=True, fused=False)
+    ms_unf = dist.max(ms_unf)
+    attn_ms = dist.max(per_unf["attn_ms"])
+    write_ms = dist.max(per_unf["write_ms"])
 
     # gather leg: rebuild contiguous K/V for the whole batch
     off = si.cu_offsets(lens)
@@ -416,9 +431,7 @@ def run_ours(args, dist):
     if not args.no_e2e:
         host_in = {"q": reps[0]["q"].cpu().pin_memory(), "kn": reps[0]["kn"].cpu().pin_memory(),
                    "vn": reps[0]["vn"].cpu().pin_memory(), "bt": torch.from_numpy(bt_shuf).pin_memory(),
-                   "lens": torch.from_numpy(lens).pin_memory(),
-                   "pos": torch.from_numpy((lens - 1).astype(np.int32)).pin_memory(),
-                   "seq": torch.from_numpy(np.arange(S, dtype=np.int32)).pin_memory()}
+                   "lens": torch.from_numpy(lens).pin_memory()}
         host_out = torch.empty((S, Hq, D), dtype=torch.float16).pin_memory()
         dev_in = {k: torch.empty_like(v, device=device) for k, v in host_in.items()}
         h2d = sum(v.numel() * v.element_size() for v in host_in.values())
@@ -429,9 +442,8 @@ def run_ours(args, dist):
             r = reps[i % R]
             for k_, v_ in host_in.items():
                 dev_in[k_].copy_(v_, non_blocking=True)
-            pkv.pf_write_kv(r["pool"], 0, dev_in["kn"], dev_in["vn"], dev_in["bt"], dev_in["seq"], dev_in["pos"])
-            pkv.pf_paged_decode_attention(r["pool"], 0, dev_in["q"], dev_in["bt"], dev_in["lens"], w["scale"],
-                                          r["out"], args.split, r["ws"])
+            pkv.pf_decode_step(r["pool"], 0, dev_in["q"], dev_in["kn"], dev_in["vn"], dev_in["bt"], dev_in["lens"],
+                               w["scale"], r["out"], args.split, r["ws"])
             host_out.copy_(r["out"], non_blocking=True)
 
         for i in range(W):
@@ -450,8 +462,8 @@ def run_ours(args, dist):
 
     peak, peak_src = read_peaks()
     step_s = ms_main / 1e3 / K
-    attn_s = attn_ms / 1e3
-    achieved = a_bytes / attn_s / 1e9
+    call_s = step_call_ms / 1e3
+    achieved = step_bytes / call_s / 1e9
     n = dist.world
     res = {
         "metric": METRIC,
@@ -470,26 +482,30 @@ def run_ours(args, dist):
         "config": {"workload": WORKLOAD_NAME, "split_tokens": args.split, "parallelism": f"replicas x{n}",
                    "l2": f"rotating {R} pool replicas ({R * pool_pair / 1e6:.0f} MB) > 3x L2 ({l2 / 1e6:.0f} MB)",
                    "step_bytes": step_bytes, "attention_bytes": a_bytes, "write_bytes": w_bytes,
-                   "tokens_in_context": int(lens.sum())},
+                   "tokens_in_context": int(lens.sum()), "step_call": "pf_decode_step (fused scatter + attention)"},
         "tokens_per_s_per_layer": round(dist.sum(S) / step_s, 1),
-        "attention_calls_per_s": round(n / attn_s, 1),
-        "pct_of_peak": {"attention_vs_measured_copy": round(achieved / peak, 4),
-                        "attention_vs_8TBs_spec": round(achieved / SPEC_HBM_GBS, 4),
-                        "step_vs_measured_copy": round(step_bytes / step_s / 1e9 / peak, 4)},
-        "per_kernel_ms": {"write_kv": round(write_ms, 5), "attention": round(attn_ms, 5),
-                          "step_with_events": round(ms_ev / K, 5)},
-        "ordered": {"ms_per_step": round(ms_ord / K, 5), "attention_ms": round(attn_ord_ms, 5),
-                    "attention_gbs": round(a_bytes / (attn_ord_ms / 1e3) / 1e9, 1),
-                    "shuffled_over_ordered_attention_time": round(attn_ms / attn_ord_ms, 4)},
+        "attention_calls_per_s": round(n / call_s, 1),
+        "pct_of_peak": {"step_vs_measured_copy": round(achieved / peak, 4),
+                        "step_vs_8TBs_spec": round(achieved / SPEC_HBM_GBS, 4)},
+        "per_call_ms": {"decode_step_fused": round(step_call_ms, 5),
+                        "steps_back_to_back": round(ms_main / K, 5),
+                        "steps_with_events": round(ms_ev / K, 5)},
+        "unfused": {"ms_per_step": round(ms_unf / K, 5), "write_kv_ms": round(write_ms, 5),
+                    "attention_ms": round(attn_ms, 5),
+                    "attention_gbs": round(a_bytes / (attn_ms / 1e3) / 1e9, 1),
+                    "attention_frac_of_measured_copy": round(a_bytes / (attn_ms / 1e3) / 1e9 / peak, 4)},
+        "ordered": {"ms_per_step": round(ms_ord / K, 5), "decode_step_ms": round(step_ord_ms, 5),
+                    "gbs": round(step_bytes / (step_ord_ms / 1e3) / 1e9, 1),
+                    "shuffled_over_ordered_time": round(step_call_ms / step_ord_ms, 4)},
         "gather": {"gbs": round(g_bytes / (gather_ms / 1e3) / 1e9, 1), "ms": round(gather_ms, 5),
                    "bytes": g_bytes, "frac_of_measured_copy": round(g_bytes / (gather_ms / 1e3) / 1e9 / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profile_traffic(),
-                     "kernel": "pf_paged_decode_attention (paged_decode_kernel<64,1,4> + merge_kernel)",
+                     "kernel": "pf_decode_step (paged_decode_kernel<64,1,4> with the fused write, + merge_kernel)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
         "e2e": e2e,
-        "gpu_launches": K * (1 + attn_launches),
+        "gpu_launches": K * attn_launches,
         "clocks": clocks,
     }
     if dist.rank == 0:

@@ -196,6 +196,25 @@ PF_API int pf_paged_decode_attention(const pf_pool *pool, int layer, const void 
                               int out_dtype, int split_tokens,
                               void *workspace, size_t ws_bytes, void *stream);
 
+/* One decode step of one layer, fused (the scatter of PageForge, "Four
+ * layers, one pointer", and the attention of the PagedAttention blog, "The
+ * Attention Kernel", in one pass): for every sequence s with
+ * L = context_lens[s] >= 1, the new token's rows k_new[s] and v_new[s]
+ * (fp16 [n_seqs][Hkv][D], device) are written to slot(s, L - 1) of layer
+ * `layer`, and then single-query attention runs over the L tokens exactly as
+ * pf_paged_decode_attention does.  Results are those of pf_write_kv with
+ * seq_idx[i] = i, pos[i] = L_i - 1 followed by pf_paged_decode_attention.
+ * The write happens inside the attention kernel, by the block that reads
+ * that slot, so a step costs one launch (plus the merge launch when a
+ * sequence is split).  Same workspace as pf_paged_decode_attention. */
+PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
+                          const void *k_new, const void *v_new,
+                          const int32_t *block_tables, int max_blocks_per_seq,
+                          const int32_t *context_lens, int n_seqs,
+                          int n_q_heads, float scale, void *out,
+                          int out_dtype, int split_tokens, void *workspace,
+                          size_t ws_bytes, void *stream);
+
 /* The decode attention call for callers that cannot allocate device memory.
  * No counterpart on the pages: it exists for code that may only touch the
  * buffers it is handed -- for instance an operator inside another runtime

@@ -15,7 +15,7 @@ from ._native import (  # noqa: F401
     Allocator, DoubleFree, OutOfBlocks, PagedKVError, Pool,
     build, lib,
     pf_abi_version, pf_alloc_blocks, pf_alloc_create, pf_alloc_destroy, pf_alloc_free_count,
-    pf_decode_workspace_bytes, pf_decode_workspace_init, pf_device_status, pf_free_blocks,
+    pf_decode_step, pf_decode_workspace_bytes, pf_decode_workspace_init, pf_device_status, pf_free_blocks,
     pf_gather_kv, pf_last_error, pf_paged_decode_attention, pf_paged_decode_attention_noalloc,
     pf_pool_bytes, pf_pool_create,
     pf_pool_destroy, pf_seq_release, pf_seq_reserve, pf_write_kv,

@@ -81,6 +81,7 @@ def lib():
         "pf_paged_decode_attention": (I, [P, I, P, P, I, P, I, I, F, P, I, I, P, Z, P]),
         "pf_device_status": (I, [ctypes.POINTER(I), I, P]),
         "pf_paged_decode_attention_noalloc": (I, [P, I, P, P, I, P, I, I, F, P, I, I, P]),
+        "pf_decode_step": (I, [P, I, P, P, P, P, I, P, I, I, F, P, I, I, P, Z, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -283,6 +284,29 @@ def pf_paged_decode_attention(pool, layer, q, block_tables, context_lens, scale,
         raise PagedKVError(PF_ERR_INVALID, "out must be float16 or float32")
     _check(lib().pf_paged_decode_attention(
         pool.handle, layer, _dev_ptr(q, "q", torch.float16), _dev_ptr(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32), n, hq, float(scale),
+        _dev_ptr(out, "out"), out_dtype, split_tokens, _dev_ptr(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+
+
+def pf_decode_step(pool, layer, q, k_new, v_new, block_tables, context_lens, scale, out, split_tokens, workspace,
+                   stream=None):
+    """Fused decode step: write each sequence's new K/V row at position
+    context_lens[s] - 1, then decode attention over the grown context."""
+    import torch
+    n, hq, d = q.shape
+    if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.numel() != n:
+        raise PagedKVError(PF_ERR_INVALID, "block_tables must be [n_seqs, max_blocks]; context_lens [n_seqs]")
+    if tuple(k_new.shape) != (n, pool.n_kv_heads, d) or tuple(v_new.shape) != tuple(k_new.shape):
+        raise PagedKVError(PF_ERR_INVALID, "k_new / v_new must be [n_seqs, n_kv_heads, head_dim]")
+    if tuple(out.shape) != (n, hq, d):
+        raise PagedKVError(PF_ERR_INVALID, "out must have the shape of q")
+    out_dtype = {torch.float16: PF_F16, torch.float32: PF_F32}.get(out.dtype)
+    if out_dtype is None:
+        raise PagedKVError(PF_ERR_INVALID, "out must be float16 or float32")
+    _check(lib().pf_decode_step(
+        pool.handle, layer, _dev_ptr(q, "q", torch.float16), _dev_ptr(k_new, "k_new", torch.float16),
+        _dev_ptr(v_new, "v_new", torch.float16), _dev_ptr(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32), n, hq, float(scale),
         _dev_ptr(out, "out"), out_dtype, split_tokens, _dev_ptr(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), _stream_ptr(stream)))

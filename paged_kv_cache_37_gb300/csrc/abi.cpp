@@ -163,12 +163,12 @@ int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
     return PF_OK;
 }
 
-int pf_paged_decode_attention(const pf_pool *pool, int layer, const void *q,
-                              const int32_t *block_tables, int max_blocks_per_seq,
-                              const int32_t *context_lens, int n_seqs, int n_q_heads, float scale,
-                              void *out, int out_dtype, int split_tokens, void *workspace,
-                              size_t ws_bytes, void *stream) {
-    pkv::clear_error();
+// Checks and launch shared by pf_paged_decode_attention (k_new = v_new =
+// null) and pf_decode_step (the fused write of the new token rows).
+static int decode_call(const pf_pool *pool, int layer, const void *q, const void *k_new, const void *v_new,
+                       const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                       int n_seqs, int n_q_heads, float scale, void *out, int out_dtype, int split_tokens,
+                       void *workspace, size_t ws_bytes, void *stream) {
     int rc = check_pool(pool, layer, "pf_paged_decode_attention");
     if (rc) return rc;
     if (n_seqs < 0) return pkv::set_error(PF_ERR_INVALID, "pf_paged_decode_attention: negative n_seqs");
@@ -206,9 +206,33 @@ int pf_paged_decode_attention(const pf_pool *pool, int layer, const void *q,
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_decode_attention: workspace has " +
                                                   std::to_string(ws_bytes) + " bytes, needs " +
                                                   std::to_string(need));
-    pkv::AttnArgs a{const_cast<pf_pool *>(pool), layer, q, block_tables, max_blocks_per_seq, context_lens,
-                    n_seqs, n_q_heads, scale, out, out_dtype, plan, workspace, ws_bytes};
+    pkv::AttnArgs a{const_cast<pf_pool *>(pool), layer, q, k_new, v_new, block_tables, max_blocks_per_seq,
+                    context_lens, n_seqs, n_q_heads, scale, out, out_dtype, plan, workspace, ws_bytes};
     return pkv::launch_attention(a, static_cast<cudaStream_t>(stream));
+}
+
+int pf_paged_decode_attention(const pf_pool *pool, int layer, const void *q, const int32_t *block_tables,
+                              int max_blocks_per_seq, const int32_t *context_lens, int n_seqs, int n_q_heads,
+                              float scale, void *out, int out_dtype, int split_tokens, void *workspace,
+                              size_t ws_bytes, void *stream) {
+    pkv::clear_error();
+    return decode_call(pool, layer, q, nullptr, nullptr, block_tables, max_blocks_per_seq, context_lens, n_seqs,
+                       n_q_heads, scale, out, out_dtype, split_tokens, workspace, ws_bytes, stream);
+}
+
+int pf_decode_step(const pf_pool *pool, int layer, const void *q, const void *k_new, const void *v_new,
+                   const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, int n_seqs,
+                   int n_q_heads, float scale, void *out, int out_dtype, int split_tokens, void *workspace,
+                   size_t ws_bytes, void *stream) {
+    pkv::clear_error();
+    if (n_seqs > 0) {
+        if (!k_new || !v_new) return pkv::set_error(PF_ERR_INVALID, "pf_decode_step: null k_new / v_new");
+        if (!aligned16(k_new) || !aligned16(v_new))
+            return pkv::set_error(PF_ERR_INVALID, "pf_decode_step: k_new / v_new must be 16-byte aligned");
+    }
+    // the same checks as pf_paged_decode_attention, then the fused launch
+    return decode_call(pool, layer, q, k_new, v_new, block_tables, max_blocks_per_seq, context_lens, n_seqs,
+                       n_q_heads, scale, out, out_dtype, split_tokens, workspace, ws_bytes, stream);
 }
 
 int pf_device_status(int *status_out, int reset, void *stream) {

@@ -200,6 +200,8 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     const AttnPlan &plan = a.plan;
 
     attn::Params p;
+    p.k_pool = static_cast<__half *>(pool->k_base);
+    p.v_pool = static_cast<__half *>(pool->v_base);
     p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + plan.counter_bytes);
     const size_t rec_bytes = plan.partial_bytes - plan.n_jobs * sizeof(attn::Job);
     p.jobs = reinterpret_cast<attn::Job *>(static_cast<uint8_t *>(a.workspace) + plan.counter_bytes + rec_bytes);
@@ -224,6 +226,9 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     for (int s0 = 0; s0 < a.n_seqs; s0 += attn::kMaxSeqsPerLaunch) {
         const int n = a.n_seqs - s0 < attn::kMaxSeqsPerLaunch ? a.n_seqs - s0 : attn::kMaxSeqsPerLaunch;
         p.q = static_cast<const __half *>(a.q) + (size_t)s0 * row;
+        const size_t kv_row = (size_t)pool->n_kv_heads * pool->head_dim;
+        p.k_new = a.k_new ? static_cast<const __half *>(a.k_new) + (size_t)s0 * kv_row : nullptr;
+        p.v_new = a.v_new ? static_cast<const __half *>(a.v_new) + (size_t)s0 * kv_row : nullptr;
         p.out = static_cast<uint8_t *>(a.out) + (size_t)s0 * row * out_elem;
         p.bt = a.block_tables + (size_t)s0 * a.max_blocks;
         p.lens = a.context_lens + s0;

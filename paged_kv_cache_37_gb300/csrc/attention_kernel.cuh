@@ -89,6 +89,13 @@ constexpr int kMaxSeqsPerLaunch = 1024;   // the span schedule keeps lengths in 
 
 struct Params {
     const __half *q;
+    // fused decode step (pf_decode_step): the new token of each sequence,
+    // [n_seqs][n_kv_heads][D], written to slot L - 1 before it is read;
+    // null for plain attention
+    const __half *k_new;
+    const __half *v_new;
+    __half *k_pool;   // pool bases (for the fused write)
+    __half *v_pool;
     void *out;
     const int32_t *bt;
     const int32_t *lens;
@@ -162,7 +169,7 @@ struct __align__(128) Smem {
 
 struct ProdItem {
     bool done;
-    int s, h0, tok0, ntok, kind, a, b, c, span, pg0, npg;
+    int s, h0, tok0, ntok, kind, a, b, c, span, pg0, npg, L;
     int ids0, ids1;   // raw block ids of pages pg0 + lane and pg0 + 32 + lane
 };
 
@@ -193,11 +200,25 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         return id;
     };
     auto finish_decode = [&](ProdItem &it, int L) {
+        it.L = L;
         it.ntok = min(it.ntok, L - it.tok0);
         it.pg0 = it.tok0 / B;
         it.npg = (it.tok0 + it.ntok - 1) / B - it.pg0 + 1;
         it.ids0 = load_id(it.s, it.pg0, it.npg, 0);
         it.ids1 = load_id(it.s, it.pg0, it.npg, 32);
+        // Fused decode step: the item that ends at the sequence's end holds
+        // its newest token; start pulling the new rows into L2 now, so the
+        // copy into the pool at the item's last tile finds them close.
+        if (p.k_new != nullptr && it.tok0 + it.ntok == L) {
+            const int nv = min(HG, p.n_kv_heads - it.h0);
+            const size_t src = ((size_t)it.s * p.n_kv_heads + it.h0) * D;
+            for (int c = lane * 8; c < nv * D; c += 32 * 8) {   // one prefetch per 128 bytes
+                if ((c & 63) == 0) {
+                    prefetch_l2(p.k_new + src + c);
+                    prefetch_l2(p.v_new + src + c);
+                }
+            }
+        }
     };
 
     // ---- chunk schedule: 32-sequence window of the chunk numbering: per lane
@@ -341,6 +362,8 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         // latency overlaps with issuing this item's tiles.
         const ProdItem nx = decode(k + 1);
 
+        const bool writes_new = p.k_new != nullptr && it.tok0 + it.ntok == it.L;
+
         int wbase = 0;
         int cur = it.ids0;
         int nxt = it.ids1;
@@ -360,6 +383,28 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
                 break;
             }
             const uint32_t full_bar = smem_addr(&sm.full[stage]);
+            if (writes_new && j == ntiles - 1) {
+                // Fused decode step: this tile holds the sequence's newest
+                // token.  Copy its rows for the heads of this group into the
+                // pool (this CTA is the only reader of those bytes), then
+                // order the writes before the tile's TMA read.
+                const int tn = it.L - 1;
+                const int raw = __shfl_sync(FULL, cur, (tn / B - it.pg0 - wbase) & 31);
+                const int nv = min(HG, p.n_kv_heads - it.h0);
+                if (raw >= 0 && raw < p.n_blocks) {
+                    const size_t row = (size_t)p.layer_row0 + (size_t)raw * B + tn % B;
+                    const size_t dst = (row * p.n_kv_heads + it.h0) * D;
+                    const size_t src = ((size_t)it.s * p.n_kv_heads + it.h0) * D;
+                    for (int c = lane; c < nv * D / 8; c += 32) {
+                        reinterpret_cast<uint4 *>(p.k_pool + dst)[c] = reinterpret_cast<const uint4 *>(p.k_new + src)[c];
+                        reinterpret_cast<uint4 *>(p.v_pool + dst)[c] = reinterpret_cast<const uint4 *>(p.v_new + src)[c];
+                    }
+                } else if (lane == 0) {
+                    atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
+                }
+                fence_proxy_async_global();
+                __syncwarp();
+            }
             if (B >= TB) {
                 // the tile is rows [t % B, t % B + TB) of one page
                 const int id = checked(__shfl_sync(FULL, cur, pa - wbase));

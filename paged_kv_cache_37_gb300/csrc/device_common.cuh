@@ -130,6 +130,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// Order this thread's earlier generic-proxy global writes before its later
+// async-proxy (TMA) accesses of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Hint: bring the 128-byte line holding p into L2.
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // L2 policy for data read exactly once per call: evict first.
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;

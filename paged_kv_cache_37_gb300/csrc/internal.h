@@ -96,6 +96,8 @@ struct AttnArgs {
     pf_pool *pool;
     int layer;
     const void *q;
+    const void *k_new;   // fused decode step: new token rows (null: attention only)
+    const void *v_new;
     const int32_t *block_tables;
     int max_blocks;
     const int32_t *context_lens;

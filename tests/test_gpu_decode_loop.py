@@ -5,7 +5,8 @@ whole demand-paged decode loop on the GPU against the oracle.
 Each step every sequence grows by one token: the product allocator appends a
 block when the last one is full (and must hand out exactly the ids the
 oracle's free-list model does), then per layer the new K/V token is scattered
-and decode attention runs over the grown context.  Attention is checked
+and decode attention runs over the grown context (two calls on even layers,
+the fused pf_decode_step on odd ones).  Attention is checked
 against the oracle at several steps; at the end the whole pool must equal the
 oracle's scatter of the same tokens, byte for byte, and every block returns to
 the free list."""
@@ -74,9 +75,13 @@ def test_gpt2_shape_demand_paged_decode(pkv, cuda_dev, oracle_mod):
             kn = rng.standard_normal((S, H, D), dtype=np.float32).astype(np.float16)
             vn = rng.standard_normal((S, H, D), dtype=np.float32).astype(np.float16)
             q = rng.standard_normal((S, H, D), dtype=np.float32).astype(np.float16)
-            pkv.pf_write_kv(pool, layer, dev(kn, cuda_dev), dev(vn, cuda_dev), bt_dev, all_seq, pos_dev)
+            if layer % 2 == 0:   # two calls: scatter, then attention
+                pkv.pf_write_kv(pool, layer, dev(kn, cuda_dev), dev(vn, cuda_dev), bt_dev, all_seq, pos_dev)
+                pkv.pf_paged_decode_attention(pool, layer, dev(q, cuda_dev), bt_dev, lens_dev, w["scale"], out, 0, ws)
+            else:                # the fused decode step
+                pkv.pf_decode_step(pool, layer, dev(q, cuda_dev), dev(kn, cuda_dev), dev(vn, cuda_dev), bt_dev,
+                                   lens_dev, w["scale"], out, 0, ws)
             oracle_mod.scatter(k_host, v_host, layer, kn, vn, bt, np.arange(S, dtype=np.int32), new_pos)
-            pkv.pf_paged_decode_attention(pool, layer, dev(q, cuda_dev), bt_dev, lens_dev, w["scale"], out, 0, ws)
             if step in CHECK_STEPS:
                 ref = oracle_mod.attention_paged(q, k_host, v_host, layer, bt, lens, w["scale"])
                 assert_close_to_oracle(host(out), ref, what=f"step {step} layer {layer}")
