@@ -148,7 +148,7 @@ def profile_traffic():
         fields = {}
         for line in open(path):
             if ":" in line and line.startswith("- "):
-                k, v = line[2:].split(":", 1)
+                k, v = line[2:].rsplit(":", 1)
                 fields[k.strip()] = v.strip().strip("`")
         if fields.get("kernel sources sha256[:16]") != kernel_sources_hash():
             return None
