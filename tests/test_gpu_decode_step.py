@@ -105,3 +105,33 @@ def test_step_bad_block_id_is_flagged_and_not_written(pkv, cuda_dev):
     changed = np.argwhere(np.any(k1.view(np.uint16) != k0.view(np.uint16), axis=(3, 4)))
     slot0 = (c.bt[0, 39 // 16], 39 % 16)
     assert {(int(b), int(r)) for _, b, r in changed} == {(int(slot0[0]), int(slot0[1]))}
+
+
+def test_back_to_back_steps_read_what_the_previous_step_wrote(pkv, cuda_dev, oracle_mod):
+    """Back-to-back steps on one layer with no synchronisation between them:
+    step i + 1 reads the pool row that step i wrote and a q that a torch
+    kernel produced just before the call; lengths change between steps by
+    host copies."""
+    import torch
+    lens = si.uniform_lengths(24, 1, 300, seed=13)
+    maxb = -(-(int(lens.max()) + 10) // 16)
+    c = PagedCase(pkv, cuda_dev, lens + 10, 8, 4, 64, 16, max_blocks=maxb)   # room for 10 more tokens
+    kh, vh = c.k_host.copy(), c.v_host.copy()
+    ws = pkv.make_workspace(c.pool, len(lens), 8, maxb, 0)
+    out = torch.empty((len(lens), 8, 64), dtype=torch.float16, device=cuda_dev)
+    cur = lens.copy()
+    live = np.arange(len(lens), dtype=np.int32)
+    for step in range(10):
+        cur = cur + 1
+        kn = si.fp16_normal((len(lens), 4, 64), 600 + 3 * step)
+        vn = si.fp16_normal((len(lens), 4, 64), 601 + 3 * step)
+        q_src = dev(si.fp16_normal((len(lens), 8, 64), 602 + 3 * step), cuda_dev)
+        lens_dev = dev(cur.astype(np.int32), cuda_dev)
+        q = q_src * 1.0            # a kernel writing q right before the call
+        pkv.pf_decode_step(c.pool, 0, q, dev(kn, cuda_dev), dev(vn, cuda_dev), c.bt_dev, lens_dev, 0.125, out, 0,
+                           ws)
+        oracle_mod.scatter(kh, vh, 0, kn, vn, c.bt, live, (cur - 1).astype(np.int32))
+        ref = oracle_mod.attention_paged(host(q_src), kh, vh, 0, c.bt, cur, 0.125)
+        assert_close_to_oracle(host(out), ref, what=f"back-to-back step {step}")
+    assert np.array_equal(host(c.k_dev).view(np.uint16), kh.view(np.uint16))
+    assert pkv.pf_device_status(reset=True) == 0
