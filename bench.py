@@ -355,9 +355,9 @@ def run_ours(args, dist):
                        "attn_ms": statistics.mean(b.elapsed_time(c) for _, b, c in evs)}
         return total_ms, per
 
-    # kernels per step: the fused grid, plus the merge grid unless sequences
-    # are never split (one launch of each per 1024 sequences)
-    attn_launches = (1 if args.split == -1 else 2) * -(-S // 1024)
+    # kernels per step: the fused grid (cut pairs are merged inside it), plus
+    # a merge grid for fixed chunks (split > 0); one of each per 1024 sequences
+    attn_launches = (2 if args.split > 0 else 1) * -(-S // 1024)
     a_bytes = attention_bytes(lens, Hq, Hkv, D, B)
     w_bytes = write_bytes(S, Hkv, D)
     step_bytes = a_bytes + w_bytes
@@ -501,7 +501,7 @@ def run_ours(args, dist):
                    "bytes": g_bytes, "frac_of_measured_copy": round(g_bytes / (gather_ms / 1e3) / 1e9 / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profile_traffic(),
-                     "kernel": "pf_decode_step (paged_decode_kernel<64,1,4> with the fused write, + merge_kernel)",
+                     "kernel": "pf_decode_step (paged_decode_kernel_r128<64,1,4>: fused write, attention, in-kernel merge)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
         "e2e": e2e,

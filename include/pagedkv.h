@@ -169,8 +169,11 @@ PF_API size_t pf_decode_workspace_bytes(const pf_pool *pool, int n_seqs,
 
 /* Prepare a workspace for first use (zero it).  Needed once after the
  * workspace is allocated: merge jobs in the workspace are recognised by a
- * per-call stamp, and zeroed memory holds no stamp of any call.  Calls leave
- * the workspace ready for the next call. */
+ * per-call stamp (zeroed memory holds no stamp of any call), and the
+ * counters that tell which block merges a split sequence must start at zero.
+ * Every call that completes leaves the workspace ready for the next one.
+ * After a call that set PF_DEV_WAIT_TIMEOUT, initialise the workspace again
+ * before reusing it. */
 PF_API int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 
 /* Single-query decode attention through the block tables (PagedAttention
@@ -205,8 +208,9 @@ PF_API int pf_paged_decode_attention(const pf_pool *pool, int layer, const void 
  * pf_paged_decode_attention does.  Results are those of pf_write_kv with
  * seq_idx[i] = i, pos[i] = L_i - 1 followed by pf_paged_decode_attention.
  * The write happens inside the attention kernel, by the block that reads
- * that slot, so a step costs one launch (plus the merge launch when a
- * sequence is split).  Same workspace as pf_paged_decode_attention. */
+ * that slot, so a step costs one launch (plus a merge launch when
+ * split_tokens > 0 cuts a sequence).  Same workspace as
+ * pf_paged_decode_attention. */
 PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
                           const void *k_new, const void *v_new,
                           const int32_t *block_tables, int max_blocks_per_seq,
@@ -230,10 +234,11 @@ PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
  * - The first call on a device looks up the array's device address (once
  *   per device, with that device current); make that first call before any
  *   stream capture.
- * - Every call on a device uses the same array and leaves its contents
- *   behind (nothing in it has to start at zero for the next call).  Calls
- *   that overlap on the GPU (other streams, other threads) race on the
- *   scratch: order them on one stream. */
+ * - Every call on a device uses the same array.  A call that completes
+ *   leaves it ready for the next one; after a call that set
+ *   PF_DEV_WAIT_TIMEOUT, pf_device_status with reset != 0 zeroes it again.
+ *   Calls that overlap on the GPU (other streams, other threads) race on
+ *   the scratch: order them on one stream. */
 PF_API int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
                                              const void *q,
                                              const int32_t *block_tables,
@@ -246,7 +251,9 @@ PF_API int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
 
 /* Read the device status word (OR of pf_device_flag bits set by kernels of
  * this library on the current device since the last reset) into *status_out.
- * Synchronises `stream`.  reset != 0 clears the word afterwards. */
+ * Synchronises `stream`.  reset != 0 clears the word afterwards and, when the
+ * word held PF_DEV_WAIT_TIMEOUT, zeroes the scratch of
+ * pf_paged_decode_attention_noalloc on this device. */
 PF_API int pf_device_status(int *status_out, int reset, void *stream);
 
 #ifdef __cplusplus

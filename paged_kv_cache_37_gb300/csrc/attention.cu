@@ -150,8 +150,9 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
         rc = resident_grid(pool, n_q_heads, &plan->grid);
         if (rc) return rc;
     }
-    // [reserved: 256 B][fp32 records][merge jobs]
+    // [reserved: 256 B][fp32 records][arrival counters][merge jobs]
     plan->counter_bytes = 256;
+    plan->arrival_bytes = 0;
     const int ng = (pool->n_kv_heads + HG - 1) / HG;
     if (plan->spans) {
         plan->chunk = TB;
@@ -161,10 +162,13 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
             grid = kGridBoundNoDevice;
         }
         // two records (first and last segment of a span) per span and head
-        // of the group; one job slot per span
+        // of the group; one arrival counter per span and head (a span is the
+        // first span of at most one cut pair).  Cut pairs are merged inside
+        // the kernel, so there are no jobs.
         const size_t spans = (size_t)grid;
-        plan->n_jobs = spans;
-        plan->partial_bytes = spans * 2 * (size_t)HG * rec_bytes + spans * sizeof(attn::Job);
+        plan->n_jobs = 0;
+        plan->arrival_bytes = spans * (size_t)HG * sizeof(unsigned);
+        plan->partial_bytes = spans * 2 * (size_t)HG * rec_bytes + plan->arrival_bytes;
     } else {
         long long c = split_tokens == -1 ? cap : ((long long)split_tokens + TB - 1) / TB * TB;
         if (c > cap) c = cap;
@@ -202,9 +206,11 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     attn::Params p;
     p.k_pool = static_cast<__half *>(pool->k_base);
     p.v_pool = static_cast<__half *>(pool->v_base);
-    p.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(a.workspace) + plan.counter_bytes);
-    const size_t rec_bytes = plan.partial_bytes - plan.n_jobs * sizeof(attn::Job);
-    p.jobs = reinterpret_cast<attn::Job *>(static_cast<uint8_t *>(a.workspace) + plan.counter_bytes + rec_bytes);
+    uint8_t *ws = static_cast<uint8_t *>(a.workspace);
+    const size_t rec_bytes = plan.partial_bytes - plan.arrival_bytes - plan.n_jobs * sizeof(attn::Job);
+    p.partials = reinterpret_cast<float *>(ws + plan.counter_bytes);
+    p.arrivals = reinterpret_cast<unsigned *>(ws + plan.counter_bytes + rec_bytes);
+    p.jobs = reinterpret_cast<attn::Job *>(ws + plan.counter_bytes + rec_bytes + plan.arrival_bytes);
     p.status = status;
     p.max_blocks = a.max_blocks;
     p.n_q_heads = a.n_q_heads;

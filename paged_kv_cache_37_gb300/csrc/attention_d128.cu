@@ -8,7 +8,10 @@ namespace {
 
 template <int G, int HG>
 KernelInfo info() {
-    return {paged_decode_kernel<128, G, HG>, sizeof(Smem<128, G, HG>), merge_kernel<128, G, HG>};
+    if constexpr (RegisterCap<128, G, HG>::k128)
+        return {paged_decode_kernel_r128<128, G, HG>, sizeof(Smem<128, G, HG>), merge_kernel<128, G, HG>};
+    else
+        return {paged_decode_kernel<128, G, HG>, sizeof(Smem<128, G, HG>), merge_kernel<128, G, HG>};
 }
 
 template <int HG>

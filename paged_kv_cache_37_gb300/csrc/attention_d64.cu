@@ -8,7 +8,10 @@ namespace {
 
 template <int G, int HG>
 KernelInfo info() {
-    return {paged_decode_kernel<64, G, HG>, sizeof(Smem<64, G, HG>), merge_kernel<64, G, HG>};
+    if constexpr (RegisterCap<64, G, HG>::k128)
+        return {paged_decode_kernel_r128<64, G, HG>, sizeof(Smem<64, G, HG>), merge_kernel<64, G, HG>};
+    else
+        return {paged_decode_kernel<64, G, HG>, sizeof(Smem<64, G, HG>), merge_kernel<64, G, HG>};
 }
 
 template <int HG>

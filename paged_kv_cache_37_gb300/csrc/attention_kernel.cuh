@@ -39,11 +39,16 @@
 //   (exact up to rounding: all terms share the reference); acc += p v.
 // * End of item: token groups merge by shuffles (and the WPH warps of a head
 //   through shared memory).  A whole pair writes `out`.  A part of a cut pair
-//   writes its record (acc[D], m, l per q-head) with plain stores, and the
-//   first part of the pair also writes a merge job stamped with the call's
-//   epoch.  merge_kernel, launched next on the stream as a programmatic
-//   dependent of this grid, merges the records of every job of this epoch
-//   with the log-sum-exp rule.  No CTA waits for another.
+//   writes its record (acc[D], m, l per q-head) with plain stores.
+//   - Span schedule: when its CTA has no items left, the part's warp counts
+//     it in the pair's arrival counter (one per pair and head; a GPU-scope
+//     fence, then a wrapping increment).  The part that draws the last count
+//     merges all of the pair's records with the log-sum-exp rule and writes
+//     `out`.  The wrap leaves every counter at zero for the next call.
+//   - Chunk schedule: chunk 0 of the pair also writes a merge job stamped
+//     with the call's epoch; merge_kernel, launched next on the stream as a
+//     programmatic dependent of this grid, merges every job of this epoch.
+//   No CTA waits for another.
 // * Every wait is bounded (1 s) and parks the thread in hardware while it
 //   waits; a timeout sets PF_DEV_WAIT_TIMEOUT and the CTA returns after
 //   waiting (bounded) for its own copies in flight.
@@ -85,6 +90,12 @@ struct Job {
     int pad;
 };
 
+// A part of a cut pair that a consumer warp finished (span schedule): the
+// pair's output location and the span records that hold its parts.
+struct PendPart {
+    int s, h0, first, z_first, n_parts;
+};
+
 constexpr int kMaxSeqsPerLaunch = 1024;   // the span schedule keeps lengths in shared memory
 
 struct Params {
@@ -100,7 +111,8 @@ struct Params {
     const int32_t *bt;
     const int32_t *lens;
     float *partials;
-    struct Job *jobs;
+    struct Job *jobs;        // chunk schedule: merge jobs for merge_kernel
+    unsigned *arrivals;      // span schedule: parts of each cut pair done, per (first span, head)
     unsigned epoch;   // this launch's stamp for merge jobs (never 0)
     int *status;
     int n_seqs;
@@ -157,6 +169,7 @@ struct __align__(128) Smem {
     uint64_t qfull[NQ];
     uint64_t qempty[NQ];
     uint64_t cbar;   // consumer-warps barrier (count NCW), used when WPH > 1
+    PendPart pend[NCW][2];   // span schedule: this warp's cut parts (record slot 0 / 1)
     int warp_tot[NTHREADS / 32];
     // span schedule: pre[s] = tiles (per group) of sequences before s, for
     // s = 0..S; rem[s] = tokens of sequence s in its last tile (1..16), so
@@ -164,6 +177,27 @@ struct __align__(128) Smem {
     int pre[kMaxSeqsPerLaunch + 1];
     uint8_t rem[kMaxSeqsPerLaunch];
 };
+
+// L2 prefetch of the first min(row, max(128, kTablePrefetchBytes / S)) bytes
+// of each block-table row, the 128-byte lines shared out over all threads
+// of the grid.  Only addresses inside the table are touched.
+constexpr long long kTablePrefetchBytes = 1 << 20;
+
+__device__ __forceinline__ void prefetch_table_rows(const Params &p) {
+    const long long row_bytes = (long long)p.max_blocks * 4;
+    long long per_row = kTablePrefetchBytes / (p.n_seqs > 0 ? p.n_seqs : 1);
+    if (per_row < 128) per_row = 128;
+    if (per_row > row_bytes) per_row = row_bytes;
+    const long long lines = (per_row + 127) / 128;
+    const long long total = lines * p.n_seqs;
+    const char *base = reinterpret_cast<const char *>(p.bt);
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long s = i / lines;
+        const long long off = (i - s * lines) * 128;
+        prefetch_l2(base + s * row_bytes + off);
+    }
+}
 
 // ------------------------------------------------------------ producer
 
@@ -177,10 +211,6 @@ template <int D, int G, int HG>
 __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p,
                                          Smem<D, G, HG> &sm, int lane) {
     constexpr int NS = Shape<D, HG>::NS;
-    if (lane == 0) {
-        prefetch_tensormap(tmk);
-        prefetch_tensormap(tmv);
-    }
     const uint64_t pol = policy_evict_first();
     const int B = p.block_size;
     const int C = p.chunk;
@@ -505,27 +535,96 @@ __device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG>
             }
         }
     }
-    if (write_job && lane == 0) {
+    if (write_job && lane == 0) {   // chunk schedule: the pair's merge job
         Job jb;
         jb.s = d.s;
         jb.h0 = d.h0;
         jb.kind = d.kind;
         jb.pad = 0;
-        size_t j;
-        if (d.kind == kChunk) {
-            jb.first = d.a;          // chunk 0 of the sequence
-            jb.z_first = 0;
-            jb.n_parts = d.c;
-            j = (size_t)d.a * p.n_groups + d.h0 / HG;
-        } else {
-            const SpanMap map((long long)sm.pre[p.n_seqs] * p.n_groups, gridDim.x);
-            jb.first = d.span;
-            jb.z_first = d.c;
-            jb.n_parts = (int)(map.owner((long long)d.a + d.b - 1) - d.span + 1);
-            j = (size_t)d.span;   // a span is the first part of at most one cut pair
-        }
+        jb.first = d.a;          // chunk 0 of the sequence
+        jb.z_first = 0;
+        jb.n_parts = d.c;
         jb.epoch = p.epoch;
-        p.jobs[j] = jb;
+        p.jobs[(size_t)d.a * p.n_groups + d.h0 / HG] = jb;
+    }
+}
+
+// Merge the n_parts records of one cut pair for kv-head h (head hl of its
+// group) with the log-sum-exp rule and write its G output rows.  Chunk
+// records are (first + i) * Hkv + h; span records ((first + i) * 2 + slot) *
+// HG + hl, where only the first span can use slot 1 (z_first).  Each lane
+// loads one part's (m, l) and, in the same round trip, every part's acc
+// values of its own dims (D / 32 of them), PB parts at a time.
+template <int D, int G, int HG>
+__device__ __forceinline__ void merge_pair(const Params &p, int kind, int first, int z_first, int n, int s, int h,
+                                           int hl, int lane) {
+    constexpr int REC = G * (D + 2);
+    constexpr int DPL = D / 32;   // dims per lane
+    constexpr int PB = 8;         // parts whose acc loads are in flight together
+    const int Hkv = p.n_kv_heads;
+    const int Hq = p.n_q_heads;
+    auto rec_of = [&](int i) -> size_t {
+        return kind == kChunk ? (size_t)(first + i) * Hkv + h
+                              : ((size_t)(first + i) * 2 + (i == 0 ? z_first : 0)) * HG + hl;
+    };
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+        float mx = -INFINITY, ls = 0.0f;
+        float a[DPL];
+#pragma unroll
+        for (int q = 0; q < DPL; ++q) a[q] = 0.0f;
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            const int i = i0 + lane;
+            float mi = -INFINITY, li = 0.0f;
+            if (i < n) {
+                const float *pc = p.partials + rec_of(i) * REC + g * (D + 2);
+                mi = __ldcg(pc + D);
+                li = __ldcg(pc + D + 1);
+            }
+            const int nb = min(32, n - i0);
+            for (int j0 = 0; j0 < nb; j0 += PB) {
+                float v[PB][DPL];
+#pragma unroll
+                for (int jj = 0; jj < PB; ++jj) {
+                    if (j0 + jj < nb) {
+                        const float *pc = p.partials + rec_of(i0 + j0 + jj) * REC + g * (D + 2);
+#pragma unroll
+                        for (int q = 0; q < DPL; ++q) v[jj][q] = __ldcg(pc + lane + 32 * q);
+                    }
+                }
+                // running reference over the batches of 32 parts
+                float bm = mi;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o));
+                const float mn = fmaxf(mx, bm);
+                if (mn > mx) {
+                    const float sc = (mx == -INFINITY) ? 0.0f : exp2f(mx - mn);
+                    ls *= sc;
+#pragma unroll
+                    for (int q = 0; q < DPL; ++q) a[q] *= sc;
+                    mx = mn;
+                }
+                const float w = (i < n && j0 == 0) ? exp2f(mi - mx) : 0.0f;
+                if (j0 == 0) ls = fmaf(w, li, ls);
+#pragma unroll
+                for (int jj = 0; jj < PB; ++jj) {
+                    const float wj = __shfl_sync(FULL, exp2f(mi - mx), j0 + jj);
+                    if (j0 + jj < nb) {
+#pragma unroll
+                        for (int q = 0; q < DPL; ++q) a[q] = fmaf(wj, v[jj][q], a[q]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
+        const float inv = 1.0f / ls;
+#pragma unroll
+        for (int q = 0; q < DPL; ++q) {
+            const size_t o = ((size_t)s * Hq + (size_t)h * G + g) * D + lane + 32 * q;
+            if (p.out_f32) static_cast<float *>(p.out)[o] = a[q] * inv;
+            else static_cast<__half *>(p.out)[o] = __float2half_rn(a[q] * inv);
+        }
     }
 }
 
@@ -558,11 +657,52 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
     uint32_t st = 0;
     uint32_t cphase = 0;
     const uint32_t cbar = smem_addr(&sm.cbar);
+    int pending = 0;   // span schedule: bit c = a cut part with record slot c awaits its count
     for (int k = 0;; ++k) {
         const int slot = k % NQ;
         if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
         const ItemDesc d = sm.desc[slot];
-        if (d.s < 0) return;
+        if (d.s < 0) {
+            if (pending) {
+                // Count this warp's cut parts in their pairs' arrivals: one
+                // fence releases the records (this warp's lanes wrote them
+                // before the __syncwarp), then both increments are in flight
+                // together.  The part that draws a pair's last count acquires
+                // and merges the pair's records.
+                __syncwarp();
+                unsigned got0 = 0, got1 = 0;
+                if (lane == 0) {
+                    fence_acq_rel_gpu();
+                    if (pending & 1) {
+                        const PendPart &pp = sm.pend[cw][0];
+                        got0 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pp.first * HG + hl,
+                                                      (unsigned)(pp.n_parts - 1));
+                    }
+                    if (pending & 2) {
+                        const PendPart &pp = sm.pend[cw][1];
+                        got1 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pp.first * HG + hl,
+                                                      (unsigned)(pp.n_parts - 1));
+                    }
+                }
+                got0 = __shfl_sync(FULL, got0, 0);
+                got1 = __shfl_sync(FULL, got1, 0);
+                const PendPart pp0 = sm.pend[cw][0];
+                const PendPart pp1 = sm.pend[cw][1];
+                const bool last0 = (pending & 1) && got0 == (unsigned)(pp0.n_parts - 1);
+                const bool last1 = (pending & 2) && got1 == (unsigned)(pp1.n_parts - 1);
+                if (last0 || last1) {
+                    if (lane == 0) fence_acq_rel_gpu();
+                    __syncwarp();
+                    if (last0)
+                        merge_pair<D, G, HG>(p, kSpanPart, pp0.first, pp0.z_first, pp0.n_parts, pp0.s, pp0.h0 + hl,
+                                             hl, lane);
+                    if (last1)
+                        merge_pair<D, G, HG>(p, kSpanPart, pp1.first, pp1.z_first, pp1.n_parts, pp1.s, pp1.h0 + hl,
+                                             hl, lane);
+                }
+            }
+            return;
+        }
         const int h = d.h0 + hl;
         const bool active = h < p.n_kv_heads;   // ragged last group: idle warps keep the protocol
 
@@ -739,18 +879,34 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
         if (d.kind == kWhole) {
             if (leader) store_whole<D, G>(p, d, h, lane, l, acc);
         } else if (leader) {
-            // the first part of a cut pair (chunk 0, or the segment that
-            // starts at the pair's first tile) also writes the merge job
-            const bool first = d.kind == kChunk ? d.b == 0 : d.tok0 == 0;
-            write_part<D, G, HG>(p, sm, d, hl, lane, first && hl == 0, m, l, acc);
+            if (d.kind == kChunk) {
+                // chunk 0 of the sequence also writes the merge job
+                write_part<D, G, HG>(p, sm, d, hl, lane, d.b == 0 && hl == 0, m, l, acc);
+            } else {
+                // Span part: write the record and note the pair; it is
+                // counted when this CTA has no items left.  The pair's parts
+                // are spans owner(a) .. owner(a + b - 1); the first uses
+                // slot 1 when the pair starts inside it.
+                write_part<D, G, HG>(p, sm, d, hl, lane, false, m, l, acc);
+                if (lane == 0) {
+                    const SpanMap map((long long)sm.pre[p.n_seqs] * p.n_groups, gridDim.x);
+                    const long long first = map.owner(d.a);
+                    PendPart pp;
+                    pp.s = d.s;
+                    pp.h0 = d.h0;
+                    pp.first = (int)first;
+                    pp.z_first = d.a == map.start(first) ? 0 : 1;
+                    pp.n_parts = (int)(map.owner((long long)d.a + d.b - 1) - first + 1);
+                    sm.pend[cw][d.c] = pp;
+                }
+                pending |= 1 << d.c;
+            }
         }
     }
 }
 
 template <int D, int G, int HG>
-__global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
-                                                                 const __grid_constant__ CUtensorMap tmv,
-                                                                 const Params p) {
+__device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p) {
     constexpr int NS = Shape<D, HG>::NS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     Smem<D, G, HG> &sm = *reinterpret_cast<Smem<D, G, HG> *>(smem_raw);
@@ -759,6 +915,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const __grid_
     // The merge grid that follows may start launching now; it waits for
     // this grid's completion before it reads anything.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Start-up is a chain of dependent memory round trips (lengths, then
+    // block ids, then the first tile).  Fetch the descriptors and the leading
+    // part of every block-table row now, so the block-id loads that follow
+    // the length scan find their lines in L2.
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(&tmk);
+        prefetch_tensormap(&tmv);
+    }
+    prefetch_table_rows(p);
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
             mbar_init(smem_addr(&sm.full[i]), 1);
@@ -813,91 +978,45 @@ __global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const __grid_
     else consumers<D, G, HG>(p, sm, warp - 1, lane);
 }
 
-// Merge the records of every job of this launch's epoch: one warp per (job
-// slot, head).  Each lane loads one part's (m, l) and, in the same round
-// trip, every part's acc values of its own dims, so a head costs about two
-// dependent memory round trips (the job, then its records).
+// Resident CTAs per SM are set by shared memory (3 at head_dim 64 with the
+// 64 KB ring, 2 at 128) and by registers.  The register file is split over
+// the SM's four sub-partitions, so 3 CTAs of 5 warps (4 warps on one
+// sub-partition) need at most 128 registers a thread.  The instances whose
+// state fits that without spilling are compiled under that cap; the others
+// get all the registers they ask for.
+template <int D, int G, int HG>
+struct RegisterCap {
+    static constexpr bool k128 = D == 64 && (G <= 2 || (HG <= 2 && G <= 3));
+};
+
+template <int D, int G, int HG>
+__global__ void __launch_bounds__(NTHREADS, 1) paged_decode_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                                 const __grid_constant__ CUtensorMap tmv,
+                                                                 const Params p) {
+    decode_attention<D, G, HG>(tmk, tmv, p);
+}
+
+template <int D, int G, int HG>
+__global__ void __maxnreg__(128) paged_decode_kernel_r128(const __grid_constant__ CUtensorMap tmk,
+                                                          const __grid_constant__ CUtensorMap tmv, const Params p) {
+    decode_attention<D, G, HG>(tmk, tmv, p);
+}
+
+// Chunk schedule: merge the records of every job of this launch's epoch, one
+// warp per (job slot, head).  A head costs about two dependent memory round
+// trips (the job, then its records).
 template <int D, int G, int HG>
 __global__ void __launch_bounds__(128, 1) merge_kernel(const Params p, int n_jobs) {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the main grid has finished
-    constexpr int REC = G * (D + 2);
-    constexpr int DPL = D / 32;   // dims per lane
-    constexpr int PB = 8;         // parts whose acc loads are in flight together
     const int lane = threadIdx.x % 32;
-    const int Hkv = p.n_kv_heads;
-    const int Hq = p.n_q_heads;
     const long long n_warps = (long long)gridDim.x * blockDim.x / 32;
     for (long long wi = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32; wi < (long long)n_jobs * HG;
          wi += n_warps) {
         const int j = (int)(wi / HG);
         const int hl = (int)(wi - (long long)j * HG);
         const Job jb = p.jobs[j];
-        if (jb.epoch != p.epoch || jb.h0 + hl >= Hkv) continue;
-        const int h = jb.h0 + hl;
-        const int n = jb.n_parts;
-        auto rec_of = [&](int i) -> size_t {
-            return jb.kind == kChunk ? (size_t)(jb.first + i) * Hkv + h
-                                     : ((size_t)(jb.first + i) * 2 + (i == 0 ? jb.z_first : 0)) * HG + hl;
-        };
-#pragma unroll 1
-        for (int g = 0; g < G; ++g) {
-            float mx = -INFINITY, ls = 0.0f;
-            float a[DPL];
-#pragma unroll
-            for (int q = 0; q < DPL; ++q) a[q] = 0.0f;
-            for (int i0 = 0; i0 < n; i0 += 32) {
-                const int i = i0 + lane;
-                float mi = -INFINITY, li = 0.0f;
-                if (i < n) {
-                    const float *pc = p.partials + rec_of(i) * REC + g * (D + 2);
-                    mi = __ldcg(pc + D);
-                    li = __ldcg(pc + D + 1);
-                }
-                const int nb = min(32, n - i0);
-                for (int j0 = 0; j0 < nb; j0 += PB) {
-                    float v[PB][DPL];
-#pragma unroll
-                    for (int jj = 0; jj < PB; ++jj) {
-                        if (j0 + jj < nb) {
-                            const float *pc = p.partials + rec_of(i0 + j0 + jj) * REC + g * (D + 2);
-#pragma unroll
-                            for (int q = 0; q < DPL; ++q) v[jj][q] = __ldcg(pc + lane + 32 * q);
-                        }
-                    }
-                    // running reference over the batches of 32 parts
-                    float bm = mi;
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o));
-                    const float mn = fmaxf(mx, bm);
-                    if (mn > mx) {
-                        const float sc = (mx == -INFINITY) ? 0.0f : exp2f(mx - mn);
-                        ls *= sc;
-#pragma unroll
-                        for (int q = 0; q < DPL; ++q) a[q] *= sc;
-                        mx = mn;
-                    }
-                    const float w = (i < n && j0 == 0) ? exp2f(mi - mx) : 0.0f;
-                    if (j0 == 0) ls = fmaf(w, li, ls);
-#pragma unroll
-                    for (int jj = 0; jj < PB; ++jj) {
-                        const float wj = __shfl_sync(FULL, exp2f(mi - mx), j0 + jj);
-                        if (j0 + jj < nb) {
-#pragma unroll
-                            for (int q = 0; q < DPL; ++q) a[q] = fmaf(wj, v[jj][q], a[q]);
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
-            const float inv = 1.0f / ls;
-#pragma unroll
-            for (int q = 0; q < DPL; ++q) {
-                const size_t o = ((size_t)jb.s * Hq + (size_t)h * G + g) * D + lane + 32 * q;
-                if (p.out_f32) static_cast<float *>(p.out)[o] = a[q] * inv;
-                else static_cast<__half *>(p.out)[o] = __float2half_rn(a[q] * inv);
-            }
-        }
+        if (jb.epoch != p.epoch || jb.h0 + hl >= p.n_kv_heads) continue;
+        merge_pair<D, G, HG>(p, jb.kind, jb.first, jb.z_first, jb.n_parts, jb.s, jb.h0 + hl, hl, lane);
     }
 }
 

@@ -110,6 +110,17 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int *p, int v) {
     return old;
 }
 
+// Wrapping increment at GPU scope, relaxed: returns the old value and stores
+// (old >= limit) ? 0 : old + 1.  With fence_acq_rel_gpu before it, it
+// releases the thread's earlier writes; with the fence after it, it acquires.
+__device__ __forceinline__ unsigned atomic_inc_relaxed_gpu(unsigned *p, unsigned limit) {
+    unsigned old;
+    asm volatile("atom.relaxed.gpu.global.inc.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(limit) : "memory");
+    return old;
+}
+
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 // 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {

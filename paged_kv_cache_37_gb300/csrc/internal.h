@@ -50,6 +50,9 @@ namespace pkv {
 // Device status word of the current device (a __device__ variable of this
 // library); kernels OR pf_device_flag bits into it.
 int *device_status_ptr();
+// Zero the no-allocation entry point's scratch on the current device, if that
+// entry point has used it (synchronous on the stream).
+int noalloc_scratch_reset(cudaStream_t stream);
 
 int encode_pool_tmaps(pf_pool *pool, int device);
 
@@ -86,8 +89,9 @@ struct AttnPlan {
     int chunk;             // chunk schedule: tokens per chunk
     int grid;              // persistent grid (0 when planned without a device)
     size_t counter_bytes;  // reserved bytes at the front of the workspace (256 B)
-    size_t partial_bytes;  // fp32 partial records, then merge jobs
-    size_t n_jobs;         // merge job slots (0: nothing is ever merged)
+    size_t partial_bytes;  // fp32 partial records, then arrival counters, then merge jobs
+    size_t arrival_bytes;  // span schedule: one u32 per (span, head of a group)
+    size_t n_jobs;         // chunk schedule: merge job slots (0: no merge kernel)
 };
 int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_blocks, int split_tokens,
                    bool need_device, AttnPlan *plan);
