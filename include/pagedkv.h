@@ -79,7 +79,7 @@ typedef struct pf_alloc pf_alloc;
 PF_API const char *pf_last_error(void);
 
 /* ABI version of this header (PF_ABI_VERSION). */
-#define PF_ABI_VERSION 1
+#define PF_ABI_VERSION 2
 PF_API int pf_abi_version(void);
 
 /* ------------------------------------------------------------- pool ---- */
@@ -210,14 +210,25 @@ PF_API int pf_paged_decode_attention(const pf_pool *pool, int layer, const void 
  * The write happens inside the attention kernel, by the block that reads
  * that slot, so a step costs one launch (plus a merge launch when
  * split_tokens > 0 cuts a sequence).  Same workspace as
- * pf_paged_decode_attention. */
+ * pf_paged_decode_attention.
+ * flags: 0, or PF_STEP_OVERLAP_PREVIOUS: the step's kernel is launched as a
+ * programmatic dependent of the kernel issued just before it on the stream.
+ * It then becomes resident while that kernel drains and reads only
+ * context_lens and block_tables (to plan its work) before waiting for it to
+ * finish; q, k_new, v_new, the pool, out and the workspace are touched only
+ * after that.  Set the flag only when the kernel issued just before this call
+ * does not write context_lens or block_tables (for instance when it is the
+ * previous layer's or step's pf_decode_step).  If the previous operation on
+ * the stream is not a kernel, the flag changes nothing.  Unknown bits give
+ * PF_ERR_INVALID. */
+enum pf_step_flags { PF_STEP_OVERLAP_PREVIOUS = 1 };
 PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
                           const void *k_new, const void *v_new,
                           const int32_t *block_tables, int max_blocks_per_seq,
                           const int32_t *context_lens, int n_seqs,
                           int n_q_heads, float scale, void *out,
                           int out_dtype, int split_tokens, void *workspace,
-                          size_t ws_bytes, void *stream);
+                          size_t ws_bytes, int flags, void *stream);
 
 /* The decode attention call for callers that cannot allocate device memory.
  * No counterpart on the pages: it exists for code that may only touch the

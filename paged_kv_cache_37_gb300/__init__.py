@@ -9,7 +9,7 @@ Nothing here computes on the CPU and nothing falls back: a call whose library
 is missing or whose CUDA launch fails raises.
 """
 from ._native import (  # noqa: F401
-    PF_DEV_BAD_BLOCK_ID, PF_DEV_BAD_LENGTH, PF_DEV_BAD_POSITION, PF_DEV_WAIT_TIMEOUT,
+    PF_DEV_BAD_BLOCK_ID, PF_DEV_BAD_LENGTH, PF_DEV_BAD_POSITION, PF_DEV_WAIT_TIMEOUT, PF_STEP_OVERLAP_PREVIOUS,
     PF_ERR_CUDA, PF_ERR_DOUBLE_FREE, PF_ERR_INVALID, PF_ERR_OOM, PF_ERR_UNSUPPORTED,
     PF_F16, PF_F32, PF_OK,
     Allocator, DoubleFree, OutOfBlocks, PagedKVError, Pool,

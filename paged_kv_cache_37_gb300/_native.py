@@ -27,6 +27,7 @@ PF_DEV_BAD_BLOCK_ID = 1
 PF_DEV_BAD_LENGTH = 2
 PF_DEV_BAD_POSITION = 4
 PF_DEV_WAIT_TIMEOUT = 8
+PF_STEP_OVERLAP_PREVIOUS = 1
 
 _lib = None
 
@@ -81,7 +82,7 @@ def lib():
         "pf_paged_decode_attention": (I, [P, I, P, P, I, P, I, I, F, P, I, I, P, Z, P]),
         "pf_device_status": (I, [ctypes.POINTER(I), I, P]),
         "pf_paged_decode_attention_noalloc": (I, [P, I, P, P, I, P, I, I, F, P, I, I, P]),
-        "pf_decode_step": (I, [P, I, P, P, P, P, I, P, I, I, F, P, I, I, P, Z, P]),
+        "pf_decode_step": (I, [P, I, P, P, P, P, I, P, I, I, F, P, I, I, P, Z, I, P]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(L, name)
@@ -290,9 +291,11 @@ def pf_paged_decode_attention(pool, layer, q, block_tables, context_lens, scale,
 
 
 def pf_decode_step(pool, layer, q, k_new, v_new, block_tables, context_lens, scale, out, split_tokens, workspace,
-                   stream=None):
+                   flags=0, stream=None):
     """Fused decode step: write each sequence's new K/V row at position
-    context_lens[s] - 1, then decode attention over the grown context."""
+    context_lens[s] - 1, then decode attention over the grown context.
+    flags=PF_STEP_OVERLAP_PREVIOUS overlaps the launch with the previous
+    kernel on the stream, which must not write context_lens or block_tables."""
     import torch
     n, hq, d = q.shape
     if block_tables.dim() != 2 or block_tables.shape[0] != n or context_lens.numel() != n:
@@ -309,7 +312,7 @@ def pf_decode_step(pool, layer, q, k_new, v_new, block_tables, context_lens, sca
         _dev_ptr(v_new, "v_new", torch.float16), _dev_ptr(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32), n, hq, float(scale),
         _dev_ptr(out, "out"), out_dtype, split_tokens, _dev_ptr(workspace, "workspace"),
-        workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
+        workspace.numel() * workspace.element_size(), int(flags), _stream_ptr(stream)))
 
 
 def pf_paged_decode_attention_noalloc(pool, layer, q, block_tables, context_lens, scale, out, split_tokens,

@@ -166,7 +166,7 @@ int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stream) {
 // Checks and launch shared by pf_paged_decode_attention (k_new = v_new =
 // null) and pf_decode_step (the fused write of the new token rows).
 static int decode_call(const pf_pool *pool, int layer, const void *q, const void *k_new, const void *v_new,
-                       const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
+                       bool overlap_previous, const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens,
                        int n_seqs, int n_q_heads, float scale, void *out, int out_dtype, int split_tokens,
                        void *workspace, size_t ws_bytes, void *stream) {
     int rc = check_pool(pool, layer, "pf_paged_decode_attention");
@@ -206,8 +206,9 @@ static int decode_call(const pf_pool *pool, int layer, const void *q, const void
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_decode_attention: workspace has " +
                                                   std::to_string(ws_bytes) + " bytes, needs " +
                                                   std::to_string(need));
-    pkv::AttnArgs a{const_cast<pf_pool *>(pool), layer, q, k_new, v_new, block_tables, max_blocks_per_seq,
-                    context_lens, n_seqs, n_q_heads, scale, out, out_dtype, plan, workspace, ws_bytes};
+    pkv::AttnArgs a{const_cast<pf_pool *>(pool), layer, q, k_new, v_new, overlap_previous, block_tables,
+                    max_blocks_per_seq, context_lens, n_seqs, n_q_heads, scale, out, out_dtype, plan, workspace,
+                    ws_bytes};
     return pkv::launch_attention(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -216,22 +217,25 @@ int pf_paged_decode_attention(const pf_pool *pool, int layer, const void *q, con
                               float scale, void *out, int out_dtype, int split_tokens, void *workspace,
                               size_t ws_bytes, void *stream) {
     pkv::clear_error();
-    return decode_call(pool, layer, q, nullptr, nullptr, block_tables, max_blocks_per_seq, context_lens, n_seqs,
+    return decode_call(pool, layer, q, nullptr, nullptr, false, block_tables, max_blocks_per_seq, context_lens, n_seqs,
                        n_q_heads, scale, out, out_dtype, split_tokens, workspace, ws_bytes, stream);
 }
 
 int pf_decode_step(const pf_pool *pool, int layer, const void *q, const void *k_new, const void *v_new,
                    const int32_t *block_tables, int max_blocks_per_seq, const int32_t *context_lens, int n_seqs,
                    int n_q_heads, float scale, void *out, int out_dtype, int split_tokens, void *workspace,
-                   size_t ws_bytes, void *stream) {
+                   size_t ws_bytes, int flags, void *stream) {
     pkv::clear_error();
+    if (flags & ~PF_STEP_OVERLAP_PREVIOUS)
+        return pkv::set_error(PF_ERR_INVALID, "pf_decode_step: unknown flags " + std::to_string(flags));
     if (n_seqs > 0) {
         if (!k_new || !v_new) return pkv::set_error(PF_ERR_INVALID, "pf_decode_step: null k_new / v_new");
         if (!aligned16(k_new) || !aligned16(v_new))
             return pkv::set_error(PF_ERR_INVALID, "pf_decode_step: k_new / v_new must be 16-byte aligned");
     }
     // the same checks as pf_paged_decode_attention, then the fused launch
-    return decode_call(pool, layer, q, k_new, v_new, block_tables, max_blocks_per_seq, context_lens, n_seqs,
+    return decode_call(pool, layer, q, k_new, v_new, (flags & PF_STEP_OVERLAP_PREVIOUS) != 0, block_tables,
+                       max_blocks_per_seq, context_lens, n_seqs,
                        n_q_heads, scale, out, out_dtype, split_tokens, workspace, ws_bytes, stream);
 }
 

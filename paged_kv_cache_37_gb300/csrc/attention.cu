@@ -240,8 +240,26 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
         p.lens = a.context_lens + s0;
         p.n_seqs = n;
         p.epoch = next_epoch();
-        ki.fn<<<plan.grid, attn::NTHREADS, ki.smem, stream>>>(pool->tmap_k[dev], pool->tmap_v[dev], p);
-        e = cudaGetLastError();
+        if (a.overlap_previous) {
+            // A programmatic dependent of the previous kernel on the stream:
+            // resident while that kernel drains; the kernel waits for it
+            // (griddepcontrol.wait) before it touches anything but the
+            // lengths and the tables.
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(plan.grid);
+            cfg.blockDim = dim3(attn::NTHREADS);
+            cfg.dynamicSmemBytes = ki.smem;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            e = cudaLaunchKernelEx(&cfg, ki.fn, pool->tmap_k[dev], pool->tmap_v[dev], p);
+        } else {
+            ki.fn<<<plan.grid, attn::NTHREADS, ki.smem, stream>>>(pool->tmap_k[dev], pool->tmap_v[dev], p);
+            e = cudaGetLastError();
+        }
         if (e != cudaSuccess) return cuda_error(e, "pf_paged_decode_attention: launch");
         if (plan.n_jobs == 0) continue;
         // merge grid: a programmatic dependent of the main grid (it launches

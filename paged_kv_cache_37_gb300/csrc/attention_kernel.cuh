@@ -357,6 +357,9 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     int posted = 0;    // item slots posted (including the final sentinel)
     bool ok = true;
     ProdItem it = decode(0);
+    // Launched as a programmatic dependent: wait for the previous kernel on
+    // the stream before the first read of q or the pool (a no-op otherwise).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int k = 0;; ++k) {
         const int slot = k % NQ;
         if (!warp_wait(smem_addr(&sm.qempty[slot]), ((k / NQ) & 1) ^ 1, p.status, lane)) break;
@@ -643,6 +646,8 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
     const int part = cw % WPH;        // which share of each tile's tokens
     const int Hq = p.n_q_heads;
 
+    // (as in the producer: the previous kernel may still be writing `out`)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // Empty (or invalid, clamped to empty) sequences get a zero output.
     for (int s = blockIdx.x; s < p.n_seqs; s += gridDim.x) {
         if (p.lens[s] <= 0) {

@@ -102,6 +102,7 @@ struct AttnArgs {
     const void *q;
     const void *k_new;   // fused decode step: new token rows (null: attention only)
     const void *v_new;
+    bool overlap_previous;   // launch as a programmatic dependent of the previous kernel
     const int32_t *block_tables;
     int max_blocks;
     const int32_t *context_lens;

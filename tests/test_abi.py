@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(pkv):
 
 
 def test_abi_version(pkv):
-    assert pkv.pf_abi_version() == 1
+    assert pkv.pf_abi_version() == 2
 
 
 def test_pool_bytes(pkv):
@@ -91,6 +91,13 @@ def test_device_calls_reject_bad_arguments_before_launch(pkv):
     assert lib.pf_paged_decode_attention(*args(split=-7)) == pkv.PF_ERR_INVALID
     assert lib.pf_decode_workspace_bytes(pool, 4, 13, 7, 0) == 0
     assert lib.pf_decode_workspace_bytes(pool, 4, 12, 7, 0) > 0
+    # decode step: unknown flag bits, null new-token rows
+    step = lambda flags=0, kn=ok: (pool, 0, ok, kn, kn, ok, 7, ok, 4, 12, ctypes.c_float(0.125), ok, 1, 0, ok,
+                                   1 << 20, flags, None)
+    assert lib.pf_decode_step(*step(flags=2)) == pkv.PF_ERR_INVALID
+    assert "flags" in pkv.pf_last_error()
+    assert lib.pf_decode_step(*step(flags=pkv.PF_STEP_OVERLAP_PREVIOUS | 4)) == pkv.PF_ERR_INVALID
+    assert lib.pf_decode_step(*step(kn=None)) == pkv.PF_ERR_INVALID
     lib.pf_pool_destroy(pool)
 
 

@@ -80,7 +80,7 @@ def test_gpt2_shape_demand_paged_decode(pkv, cuda_dev, oracle_mod):
                 pkv.pf_paged_decode_attention(pool, layer, dev(q, cuda_dev), bt_dev, lens_dev, w["scale"], out, 0, ws)
             else:                # the fused decode step
                 pkv.pf_decode_step(pool, layer, dev(q, cuda_dev), dev(kn, cuda_dev), dev(vn, cuda_dev), bt_dev,
-                                   lens_dev, w["scale"], out, 0, ws)
+                                   lens_dev, w["scale"], out, 0, ws, flags=pkv.PF_STEP_OVERLAP_PREVIOUS)
             oracle_mod.scatter(k_host, v_host, layer, kn, vn, bt, np.arange(S, dtype=np.int32), new_pos)
             if step in CHECK_STEPS:
                 ref = oracle_mod.attention_paged(q, k_host, v_host, layer, bt, lens, w["scale"])

@@ -107,31 +107,47 @@ def test_step_bad_block_id_is_flagged_and_not_written(pkv, cuda_dev):
     assert {(int(b), int(r)) for _, b, r in changed} == {(int(slot0[0]), int(slot0[1]))}
 
 
-def test_back_to_back_steps_read_what_the_previous_step_wrote(pkv, cuda_dev, oracle_mod):
-    """Back-to-back steps on one layer with no synchronisation between them:
-    step i + 1 reads the pool row that step i wrote and a q that a torch
-    kernel produced just before the call; lengths change between steps by
-    host copies."""
+@pytest.mark.parametrize("flags", [0, 1])
+def test_back_to_back_steps_read_what_the_previous_step_wrote(pkv, cuda_dev, oracle_mod, flags):
+    """Ten steps of two layers, the layers' calls back to back on the stream
+    (with flags=PF_STEP_OVERLAP_PREVIOUS the second launch overlaps the
+    first), sharing one workspace.  Each step reads the rows the previous
+    step wrote; lengths change between steps by host copies; sequence 5 stays
+    empty, so its output rows must stay zero."""
     import torch
-    lens = si.uniform_lengths(24, 1, 300, seed=13)
+    S, Hq, Hkv, D = 24, 8, 4, 64
+    lens = si.uniform_lengths(S, 1, 300, seed=13)
+    lens[5] = 0
+    grow = np.ones(S, dtype=np.int32)
+    grow[5] = 0
     maxb = -(-(int(lens.max()) + 10) // 16)
-    c = PagedCase(pkv, cuda_dev, lens + 10, 8, 4, 64, 16, max_blocks=maxb)   # room for 10 more tokens
+    c = PagedCase(pkv, cuda_dev, lens + 10 * grow, Hq, Hkv, D, 16, max_blocks=maxb, n_layers=2)
     kh, vh = c.k_host.copy(), c.v_host.copy()
-    ws = pkv.make_workspace(c.pool, len(lens), 8, maxb, 0)
-    out = torch.empty((len(lens), 8, 64), dtype=torch.float16, device=cuda_dev)
+    ws = pkv.make_workspace(c.pool, S, Hq, maxb, 0)
+    outs = [torch.full((S, Hq, D), float("nan"), dtype=torch.float16, device=cuda_dev) for _ in range(2)]
     cur = lens.copy()
-    live = np.arange(len(lens), dtype=np.int32)
+    live = np.flatnonzero(grow).astype(np.int32)
     for step in range(10):
-        cur = cur + 1
-        kn = si.fp16_normal((len(lens), 4, 64), 600 + 3 * step)
-        vn = si.fp16_normal((len(lens), 4, 64), 601 + 3 * step)
-        q_src = dev(si.fp16_normal((len(lens), 8, 64), 602 + 3 * step), cuda_dev)
+        cur = cur + grow
         lens_dev = dev(cur.astype(np.int32), cuda_dev)
-        q = q_src * 1.0            # a kernel writing q right before the call
-        pkv.pf_decode_step(c.pool, 0, q, dev(kn, cuda_dev), dev(vn, cuda_dev), c.bt_dev, lens_dev, 0.125, out, 0,
-                           ws)
-        oracle_mod.scatter(kh, vh, 0, kn, vn, c.bt, live, (cur - 1).astype(np.int32))
-        ref = oracle_mod.attention_paged(host(q_src), kh, vh, 0, c.bt, cur, 0.125)
-        assert_close_to_oracle(host(out), ref, what=f"back-to-back step {step}")
+        ins = []
+        for layer in range(2):
+            seed = 600 + 10 * step + 5 * layer
+            kn = si.fp16_normal((S, Hkv, D), seed)
+            vn = si.fp16_normal((S, Hkv, D), seed + 1)
+            q = si.fp16_normal((S, Hq, D), seed + 2)
+            ins.append((kn, vn, q, dev(kn, cuda_dev), dev(vn, cuda_dev), dev(q, cuda_dev)))
+        for layer in range(2):
+            kn, vn, q, kn_d, vn_d, q_d = ins[layer]
+            pkv.pf_decode_step(c.pool, layer, q_d, kn_d, vn_d, c.bt_dev, lens_dev, 0.125, outs[layer], 0, ws,
+                               flags=flags)
+        for layer in range(2):
+            kn, vn, q, *_ = ins[layer]
+            oracle_mod.scatter(kh, vh, layer, kn[live], vn[live], c.bt, live, (cur[live] - 1).astype(np.int32))
+            ref = oracle_mod.attention_paged(q, kh, vh, layer, c.bt, cur, 0.125)
+            got = host(outs[layer])
+            assert np.all(got[5] == 0)
+            assert_close_to_oracle(got, ref, what=f"step {step} layer {layer} flags {flags}")
     assert np.array_equal(host(c.k_dev).view(np.uint16), kh.view(np.uint16))
+    assert np.array_equal(host(c.v_dev).view(np.uint16), vh.view(np.uint16))
     assert pkv.pf_device_status(reset=True) == 0
