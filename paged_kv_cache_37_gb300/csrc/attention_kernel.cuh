@@ -37,6 +37,11 @@
 //   shuffles; the softmax is an fp32 online softmax in the log2 domain whose
 //   reference maximum is only raised when a score passes it by more than 2^8
 //   (exact up to rounding: all terms share the reference); acc += p v.
+// * Fused decode step (k_new != null): the item that holds a sequence's
+//   token L - 1 also bulk-copies that token's new K and V rows next to q.
+//   The consumers use them in place of the tile's row L - 1 and write them
+//   into the token's pool slot with plain stores; no other block reads that
+//   slot in the launch, so nothing waits for the write.
 // * End of item: token groups merge by shuffles (and the WPH warps of a head
 //   through shared memory).  A whole pair writes `out`.  A part of a cut pair
 //   writes its record (acc[D], m, l per q-head) with plain stores.
@@ -78,7 +83,9 @@ struct ItemDesc {
     int b;      // kChunk: chunk index in the sequence; kSpanPart: tiles of the pair
     int c;      // kChunk: chunks of the sequence; kSpanPart: record slot (0/1) in the span
     int span;   // kSpanPart: span index
-    int pad0, pad1, pad2;
+    int newrow;   // fused step: token L - 1 when this item holds it, else -1
+    int newslot;  // fused step: pool row of token L - 1 (-1: bad block id, not written)
+    int pad0;
 };
 
 // A cut pair to merge: records first .. first + n_parts - 1 (chunk records
@@ -101,8 +108,8 @@ constexpr int kMaxSeqsPerLaunch = 1024;   // the span schedule keeps lengths in 
 struct Params {
     const __half *q;
     // fused decode step (pf_decode_step): the new token of each sequence,
-    // [n_seqs][n_kv_heads][D], written to slot L - 1 before it is read;
-    // null for plain attention
+    // [n_seqs][n_kv_heads][D]: attended to as token L - 1 and written to
+    // that token's pool slot; null for plain attention
     const __half *k_new;
     const __half *v_new;
     __half *k_pool;   // pool bases (for the fused write)
@@ -162,6 +169,7 @@ struct __align__(128) Smem {
     __half k[NS][Shape<D, HG>::STAGE_HALVES];
     __half v[NS][Shape<D, HG>::STAGE_HALVES];
     __half q[NQ][HG * G * D];
+    __half knew[NQ][2][HG * D];   // fused step: the new token's K and V rows of the item's heads
     float red[Shape<D, HG>::WPH > 1 ? NCW : 1][G][D + 2];   // per consumer warp: acc[D], m, l
     ItemDesc desc[NQ];
     uint64_t full[NS];
@@ -204,6 +212,7 @@ __device__ __forceinline__ void prefetch_table_rows(const Params &p) {
 struct ProdItem {
     bool done;
     int s, h0, tok0, ntok, kind, a, b, c, span, pg0, npg, L;
+    int last_id;      // fused step: raw block id of token L - 1 when the item holds it
     int ids0, ids1;   // raw block ids of pages pg0 + lane and pg0 + 32 + lane
 };
 
@@ -237,18 +246,9 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         it.ids0 = load_id(it.s, it.pg0, it.npg, 0);
         it.ids1 = load_id(it.s, it.pg0, it.npg, 32);
         // Fused decode step: the item that ends at the sequence's end holds
-        // its newest token; start pulling the new rows into L2 now, so the
-        // copy into the pool at the item's last tile finds them close.
-        if (p.k_new != nullptr && it.tok0 + it.ntok == L) {
-            const int nv = min(HG, p.n_kv_heads - it.h0);
-            const size_t src = ((size_t)it.s * p.n_kv_heads + it.h0) * D;
-            for (int c = lane * 8; c < nv * D; c += 32 * 8) {   // one prefetch per 128 bytes
-                if ((c & 63) == 0) {
-                    prefetch_l2(p.k_new + src + c);
-                    prefetch_l2(p.v_new + src + c);
-                }
-            }
-        }
+        // its newest token; its page's block id is needed when it is posted.
+        it.last_id = (p.k_new != nullptr && it.tok0 + it.ntok == L)
+                         ? p.bt[(size_t)it.s * p.max_blocks + (L - 1) / B] : 0;
     };
 
     // ---- chunk schedule: 32-sequence window of the chunk numbering: per lane
@@ -382,20 +382,38 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
             d.b = it.b;
             d.c = it.c;
             d.span = it.span;
+            // Fused decode step: the item holding token L - 1 also brings
+            // that token's K and V rows (with q, on the same barrier); the
+            // consumers use them for row L - 1 and write them to the pool.
+            const bool writes_new = p.k_new != nullptr && it.tok0 + it.ntok == it.L;
+            d.newrow = writes_new ? it.L - 1 : -1;
+            d.newslot = -1;
+            if (writes_new) {
+                if (it.last_id >= 0 && it.last_id < p.n_blocks)
+                    d.newslot = p.layer_row0 + it.last_id * B + (it.L - 1) % B;
+                else
+                    atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);   // attended to, not written
+            }
+            d.pad0 = 0;
             sm.desc[slot] = d;
             const int nv = min(HG, p.n_kv_heads - it.h0);           // heads that exist
             const uint32_t qbytes = (uint32_t)nv * G * D * 2;
-            mbar_arrive_expect_tx(smem_addr(&sm.qfull[slot]), qbytes);
+            const uint32_t rowbytes = (uint32_t)nv * D * 2;
+            const uint32_t qfull = smem_addr(&sm.qfull[slot]);
+            mbar_arrive_expect_tx(qfull, qbytes + (writes_new ? 2 * rowbytes : 0));
             bulk_load(smem_addr(sm.q[slot]), p.q + ((size_t)it.s * p.n_q_heads + (size_t)it.h0 * G) * D, qbytes,
-                      smem_addr(&sm.qfull[slot]));
+                      qfull);
+            if (writes_new) {
+                const size_t src = ((size_t)it.s * p.n_kv_heads + it.h0) * D;
+                bulk_load(smem_addr(sm.knew[slot][0]), p.k_new + src, rowbytes, qfull);
+                bulk_load(smem_addr(sm.knew[slot][1]), p.v_new + src, rowbytes, qfull);
+            }
         }
         ++posted;
 
         // The next item's numbering and block ids are requested now; their
         // latency overlaps with issuing this item's tiles.
         const ProdItem nx = decode(k + 1);
-
-        const bool writes_new = p.k_new != nullptr && it.tok0 + it.ntok == it.L;
 
         int wbase = 0;
         int cur = it.ids0;
@@ -416,28 +434,6 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
                 break;
             }
             const uint32_t full_bar = smem_addr(&sm.full[stage]);
-            if (writes_new && j == ntiles - 1) {
-                // Fused decode step: this tile holds the sequence's newest
-                // token.  Copy its rows for the heads of this group into the
-                // pool (this CTA is the only reader of those bytes), then
-                // order the writes before the tile's TMA read.
-                const int tn = it.L - 1;
-                const int raw = __shfl_sync(FULL, cur, (tn / B - it.pg0 - wbase) & 31);
-                const int nv = min(HG, p.n_kv_heads - it.h0);
-                if (raw >= 0 && raw < p.n_blocks) {
-                    const size_t row = (size_t)p.layer_row0 + (size_t)raw * B + tn % B;
-                    const size_t dst = (row * p.n_kv_heads + it.h0) * D;
-                    const size_t src = ((size_t)it.s * p.n_kv_heads + it.h0) * D;
-                    for (int c = lane; c < nv * D / 8; c += 32) {
-                        reinterpret_cast<uint4 *>(p.k_pool + dst)[c] = reinterpret_cast<const uint4 *>(p.k_new + src)[c];
-                        reinterpret_cast<uint4 *>(p.v_pool + dst)[c] = reinterpret_cast<const uint4 *>(p.v_new + src)[c];
-                    }
-                } else if (lane == 0) {
-                    atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
-                }
-                fence_proxy_async_global();
-                __syncwarp();
-            }
             if (B >= TB) {
                 // the tile is rows [t % B, t % B + TB) of one page
                 const int id = checked(__shfl_sync(FULL, cur, pa - wbase));
@@ -721,6 +717,20 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
 #pragma unroll
             for (int i = 0; i < 8; ++i) qf[g][i] = active ? qf[g][i] * p.scale_log2 : 0.0f;
         }
+        // Fused decode step: the new token's rows stand in for the tile's row
+        // L - 1 (whatever the tile read there), and the first warp of each
+        // head writes them into the pool slot.  No other block reads that
+        // slot in this launch, so the write needs no ordering here.
+        uint4 nk = make_uint4(0u, 0u, 0u, 0u), nvv = nk;
+        if (d.newrow >= 0 && active) {
+            nk = *reinterpret_cast<const uint4 *>(&sm.knew[slot][0][hl * D + sub * 8]);
+            nvv = *reinterpret_cast<const uint4 *>(&sm.knew[slot][1][hl * D + sub * 8]);
+            if (part == 0 && grp == 0 && d.newslot >= 0) {
+                const size_t dst = ((size_t)d.newslot * p.n_kv_heads + h) * D + sub * 8;
+                *reinterpret_cast<uint4 *>(p.k_pool + dst) = nk;
+                *reinterpret_cast<uint4 *>(p.v_pool + dst) = nvv;
+            }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.qempty[slot]));
 
@@ -743,13 +753,16 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 const __half *vt = sm.v[stage];
                 const int tile0 = d.tok0 + j * TB;
                 const bool ragged = tile0 + TB > tend;     // only the last tile of an item
+                const int newr = (d.newrow >= 0 && j == ntiles - 1) ? d.newrow - tile0 : -1;   // row of token L - 1
                 // phase 1: this lane group's scores for all of the warp's steps
                 // (independent chains: loads, dots and shuffles interleave)
                 uint4 kraw[STEPS];
 #pragma unroll
-                for (int step = 0; step < STEPS; ++step)
+                for (int step = 0; step < STEPS; ++step) {
                     kraw[step] = *reinterpret_cast<const uint4 *>(
                         kt + ((part * TPT + step * TPW + grp) * HG + hl) * D + sub * 8);
+                    if (part * TPT + step * TPW + grp == newr) kraw[step] = nk;
+                }
                 float z[STEPS][G];
 #pragma unroll
                 for (int step = 0; step < STEPS; ++step) {
@@ -801,9 +814,11 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 // phase 3: weights and the weighted sum of V
                 uint4 vraw[STEPS];
 #pragma unroll
-                for (int step = 0; step < STEPS; ++step)
+                for (int step = 0; step < STEPS; ++step) {
                     vraw[step] = *reinterpret_cast<const uint4 *>(
                         vt + ((part * TPT + step * TPW + grp) * HG + hl) * D + sub * 8);
+                    if (part * TPT + step * TPW + grp == newr) vraw[step] = nvv;
+                }
 #pragma unroll
                 for (int step = 0; step < STEPS; ++step) {
                     float vf[8];
