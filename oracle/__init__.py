@@ -52,6 +52,9 @@ def _load():
         "or_slot": (i64, [P, i64, i64]),
         "or_scatter": (None, [P, P, i32, i32, i32, i32, i32, P, P, P, i32, P, P, i32]),
         "or_gather": (None, [P, P, i32, i32, i32, i32, i32, P, i32, P, P, i32, P, P]),
+        "or_copy_blocks": (None, [P, P, i32, i32, i64, P, P, i32]),
+        "or_swap_out": (None, [P, P, i32, i32, i64, P, i32, P]),
+        "or_swap_in": (None, [P, P, i32, i32, i64, P, P, i32]),
         "or_attention_contiguous": (i32, [P, P, P, P, P, i32, i32, i32, i32, f32, P]),
         "or_attention_paged": (i32, [P, P, P, i32, i32, i32, i32, i32, P, i32, P, i32, i32, f32, P]),
         "or_attention_partial": (None, [P, P, P, i64, i64, i32, f32, i64, i64, P, P, P]),
@@ -144,6 +147,41 @@ def gather(k_pool, v_pool, layer, block_tables, context_lens, cu_off):
                       layer, _ptr(bt), bt.shape[1], _ptr(lens), _ptr(off), lens.size,
                       _ptr(k_out), _ptr(v_out))
     return k_out.view(np.float16), v_out.view(np.float16)
+
+
+# ------------------------------------------------- block copies, swap
+
+def copy_blocks(k_pool, v_pool, src, dst):
+    """In place: block dst[i] := block src[i] in every layer of host pools
+    [n_layers, N, B, H, D] (fp16)."""
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    n_layers, n_blocks = k_pool.shape[:2]
+    block_elems = int(np.prod(k_pool.shape[2:]))
+    s, d = _i32(src), _i32(dst)
+    _load().or_copy_blocks(_ptr(_u16(k_pool)), _ptr(_u16(v_pool)), n_layers, n_blocks, block_elems,
+                           _ptr(s), _ptr(d), s.size)
+
+
+def swap_out(k_pool, v_pool, ids):
+    """Host images [n, n_layers, 2, B, H, D] (fp16) of blocks ids."""
+    n_layers, n_blocks = k_pool.shape[:2]
+    block_elems = int(np.prod(k_pool.shape[2:]))
+    i = _i32(ids)
+    images = np.zeros((i.size, n_layers, 2) + tuple(k_pool.shape[2:]), dtype=np.uint16)
+    _load().or_swap_out(_ptr(_u16(k_pool)), _ptr(_u16(v_pool)), n_layers, n_blocks, block_elems,
+                        _ptr(i), i.size, _ptr(images))
+    return images.view(np.float16)
+
+
+def swap_in(k_pool, v_pool, images, ids):
+    """In place: blocks ids take the contents of host images [n, n_layers, 2, ...]."""
+    assert k_pool.flags.c_contiguous and v_pool.flags.c_contiguous
+    n_layers, n_blocks = k_pool.shape[:2]
+    block_elems = int(np.prod(k_pool.shape[2:]))
+    i = _i32(ids)
+    img = _u16(images)
+    _load().or_swap_in(_ptr(_u16(k_pool)), _ptr(_u16(v_pool)), n_layers, n_blocks, block_elems,
+                       _ptr(img), _ptr(i), i.size)
 
 
 # ------------------------------------------------------------ attention

@@ -17,6 +17,16 @@ What it models
   gets ``ceil(new_len/B) - ceil(cur_len/B)`` new blocks appended to its table
   row; tokens go into the last block while it has room (PagedAttention blog,
   "Architecture").
+* Shared blocks (PagedAttention blog, "Copy-on-Write for Parallel
+  Sampling"): a reference count per block tracks the sequences whose tables
+  point at it.  ``alloc`` gives a block one reference, ``share`` (a fork:
+  the child's table points at the parent's blocks) adds one, and ``free``
+  drops one per listed id; a block goes back on the stack when its last
+  reference goes, in list order.  Before a write into a block that other
+  sequences still reference, ``cow`` gives the writer a fresh block (the
+  caller copies the contents), moves one reference from the old block to it
+  and patches only the writer's table entry -- fork()'s copy-on-write.
+  Listing a block more times than it has references is a double free.
 * A "shuffled" pool (what a pool looks like after churn, PageFault README,
   "Four stages") permutes the initial hand-out order with a Fisher-Yates
   shuffle driven by SplitMix64 (Steele, Lea and Flood, "Fast splittable
@@ -71,10 +81,17 @@ class FreeListModel:
     def __init__(self, n_blocks, shuffle_seed=0):
         self.n_blocks = n_blocks
         self.stack = list(reversed(hand_out_order(n_blocks, shuffle_seed)))
-        self.owned = [False] * n_blocks
+        self.refs = [0] * n_blocks      # references per block; 0 = free
+
+    @property
+    def owned(self):
+        return [r > 0 for r in self.refs]
 
     def free_count(self):
         return len(self.stack)
+
+    def refcount(self, b):
+        return self.refs[b]
 
     def alloc(self, n):
         if n < 0:
@@ -83,18 +100,50 @@ class FreeListModel:
             raise OutOfBlocks(f"need {n} blocks, {len(self.stack)} free")
         ids = [self.stack.pop() for _ in range(n)]
         for b in ids:
-            self.owned[b] = True
+            self.refs[b] = 1
         return ids
 
     def free(self, ids):
-        seen = set()
+        listed = {}
         for b in ids:
-            if not (0 <= b < self.n_blocks) or not self.owned[b] or b in seen:
-                raise DoubleFree(f"block {b} is not allocated")
-            seen.add(b)
+            listed[b] = listed.get(b, 0) + 1
+            if not (0 <= b < self.n_blocks) or listed[b] > self.refs[b]:
+                raise DoubleFree(f"block {b} is not allocated (or listed more often than it is referenced)")
         for b in ids:
-            self.owned[b] = False
-            self.stack.append(b)
+            self.refs[b] -= 1
+            if self.refs[b] == 0:
+                self.stack.append(b)
+
+    def share(self, ids):
+        for b in ids:
+            if not (0 <= b < self.n_blocks) or self.refs[b] == 0:
+                raise ValueError(f"block {b} is not allocated")
+        for b in ids:
+            self.refs[b] += 1
+
+    def cow(self, table_row, j):
+        """Make table_row[j] private before a write into it.  Returns None when
+        the block has no other reference, else (old block, new block); the
+        caller copies the old block's contents into the new one."""
+        b = table_row[j]
+        if not (0 <= b < self.n_blocks) or self.refs[b] == 0:
+            raise ValueError(f"block {b} is not allocated")
+        if self.refs[b] == 1:
+            return None
+        if not self.stack:
+            raise OutOfBlocks("need 1 block, 0 free")
+        d = self.stack.pop()
+        self.refs[d] = 1
+        self.refs[b] -= 1
+        table_row[j] = d
+        return b, d
+
+    def seq_fork(self, parent_row, block_size, length):
+        """A child sequence that shares the parent's first `length` tokens."""
+        n = -(-length // block_size)
+        child = list(parent_row[:n])
+        self.share(child)
+        return child
 
     def seq_reserve(self, table_row, block_size, cur_len, new_len):
         """Grow a sequence's table row from cur_len to new_len tokens."""

@@ -145,6 +145,64 @@ void or_gather(const uint16_t *k_pool, const uint16_t *v_pool, int n_blocks,
     }
 }
 
+/* ------------------------------------------------- block copies, swap */
+
+/* Offset of block `block` of layer `layer` in a pool [n_layers][N][block_elems]. */
+static int64_t block_offset(int64_t layer, int64_t n_blocks, int64_t block,
+                            int64_t block_elems)
+{
+    return (layer * n_blocks + block) * block_elems;
+}
+
+/* Copy-on-write copies (PagedAttention blog, "Copy-on-Write for Parallel
+ * Sampling": a new physical block receives the contents of the shared one).
+ * For i < n, block dst[i] takes the contents of block src[i], in every layer,
+ * K and V.  block_elems = B * Hkv * D. */
+void or_copy_blocks(uint16_t *k_pool, uint16_t *v_pool, int n_layers,
+                    int n_blocks, int64_t block_elems, const int32_t *src,
+                    const int32_t *dst, int n)
+{
+    for (int i = 0; i < n; ++i) {
+        for (int layer = 0; layer < n_layers; ++layer) {
+            int64_t from = block_offset(layer, n_blocks, src[i], block_elems);
+            int64_t to = block_offset(layer, n_blocks, dst[i], block_elems);
+            memcpy(k_pool + to, k_pool + from, block_elems * sizeof(uint16_t));
+            memcpy(v_pool + to, v_pool + from, block_elems * sizeof(uint16_t));
+        }
+    }
+}
+
+/* Swapping (same blog, "Preemption and Swapping": blocks are evicted to CPU
+ * memory one by one and copied back later).  The host image of block ids[i]
+ * is images[i][layer][kv][block_elems], kv = 0 for K and 1 for V. */
+void or_swap_out(const uint16_t *k_pool, const uint16_t *v_pool, int n_layers,
+                 int n_blocks, int64_t block_elems, const int32_t *ids, int n,
+                 uint16_t *images)
+{
+    for (int i = 0; i < n; ++i) {
+        for (int layer = 0; layer < n_layers; ++layer) {
+            int64_t from = block_offset(layer, n_blocks, ids[i], block_elems);
+            uint16_t *img = images + (((int64_t)i * n_layers + layer) * 2) * block_elems;
+            memcpy(img, k_pool + from, block_elems * sizeof(uint16_t));
+            memcpy(img + block_elems, v_pool + from, block_elems * sizeof(uint16_t));
+        }
+    }
+}
+
+void or_swap_in(uint16_t *k_pool, uint16_t *v_pool, int n_layers, int n_blocks,
+                int64_t block_elems, const uint16_t *images, const int32_t *ids,
+                int n)
+{
+    for (int i = 0; i < n; ++i) {
+        for (int layer = 0; layer < n_layers; ++layer) {
+            int64_t to = block_offset(layer, n_blocks, ids[i], block_elems);
+            const uint16_t *img = images + (((int64_t)i * n_layers + layer) * 2) * block_elems;
+            memcpy(k_pool + to, img, block_elems * sizeof(uint16_t));
+            memcpy(v_pool + to, img + block_elems, block_elems * sizeof(uint16_t));
+        }
+    }
+}
+
 /* ------------------------------------------------------------ attention */
 
 /* One query row against L key/value rows given by pointer arrays.

@@ -109,3 +109,91 @@ def test_demand_paging_appends_only_when_last_block_is_full():
     assert row == [0, 1, 2, 3]
     with pytest.raises(ValueError):
         a.seq_reserve(row, 16, 64, 65)
+
+
+def _cow_golden():
+    g = {}
+    for row in read_golden("copy_on_write.txt"):
+        g.setdefault(row[0], []).append(row[1:])
+    return g
+
+
+def test_copy_on_write_example_tables():
+    """The three sequences of the copy-on-write example, built by forking the
+    prefix: the model reproduces the printed tables id for id, counts three
+    references on each shared block, and a write into a shared block changes
+    only the writer's table."""
+    g = _cow_golden()
+    B = int(g["block_size"][0][0])
+    prefix = int(g["prefix_tokens"][0][0])
+    want = {row[0]: [int(x) for x in row[1:]] for row in g["table"]}
+    shared = [int(x) for x in g["shared"][0]]
+    a = FreeListModel(16)
+    a.free(a.alloc(16))                      # every block free again ...
+    a.alloc(16)
+    a.free([0, 9, 5, 2, 13, 7])              # ... so the stack hands out 7, 13, 2, 5, 9, then 0
+    tab_a = a.alloc(prefix // B)             # the prompt's blocks
+    tab_a += a.alloc(1)                      # A's first own block
+    tab_b = a.seq_fork(tab_a, B, prefix) + a.alloc(1)
+    tab_c = a.seq_fork(tab_a, B, prefix) + a.alloc(1)
+    assert {"A": tab_a, "B": tab_b, "C": tab_c} == want
+    assert [a.refcount(b) for b in shared] == [3, 3]
+    assert [a.refcount(t[-1]) for t in (tab_a, tab_b, tab_c)] == [1, 1, 1]
+    # B writes into block 13: a new block for B only
+    before_a, before_c = list(tab_a), list(tab_c)
+    old, new = a.cow(tab_b, 1)
+    assert old == 13 and tab_b == [7, new, 5] and new == 0
+    assert tab_a == before_a and tab_c == before_c
+    assert a.refcount(13) == 2 and a.refcount(new) == 1
+    # a private block needs no copy
+    assert a.cow(tab_b, 2) is None and tab_b[2] == 5
+
+
+def test_beam_search_prefix_saving():
+    """Beam width 4 over a 1024-token prefix: the prefix is stored once, so
+    3 of its 4 copies are eliminated."""
+    g = _cow_golden()
+    B = int(g["block_size"][0][0])
+    width = int(g["beam_width"][0][0])
+    tokens = int(g["beam_prefix_tokens"][0][0])
+    n = tokens // B
+    a = FreeListModel(4 * n)
+    root = a.alloc(n)
+    beams = [root] + [a.seq_fork(root, B, tokens) for _ in range(width - 1)]
+    used = 4 * n - a.free_count()
+    assert used == n
+    assert (width * n - used) // n == int(g["copies_eliminated"][0][0])
+    assert all(a.refcount(b) == width for b in root)
+    # the prefix returns to the pool only with its last beam
+    for i, t in enumerate(beams):
+        a.free(t)
+        assert a.free_count() == (4 * n if i == width - 1 else 3 * n)
+
+
+def test_shared_frees_and_double_free():
+    a = FreeListModel(8)
+    x = a.alloc(2)
+    a.share(x)
+    a.share([x[0]])
+    assert [a.refcount(b) for b in x] == [3, 2]
+    # listing a block more often than it is referenced: error, no change
+    with pytest.raises(DoubleFree):
+        a.free([x[1], x[1], x[1]])
+    assert [a.refcount(b) for b in x] == [3, 2] and a.free_count() == 6
+    # a block returns to the stack when its last reference goes, in list order
+    a.free([x[1], x[0], x[1], x[0]])
+    assert a.refcount(x[0]) == 1 and a.stack[-1] == x[1]
+    a.free([x[0]])
+    assert a.stack[-2:] == [x[1], x[0]] and a.free_count() == 8
+    with pytest.raises(ValueError):
+        a.share([x[0]])                      # free blocks cannot be shared
+
+
+def test_cow_without_free_blocks_changes_nothing():
+    a = FreeListModel(3)
+    x = a.alloc(3)
+    a.share([x[0]])
+    row = [x[0]]
+    with pytest.raises(OutOfBlocks):
+        a.cow(row, 0)
+    assert row == [x[0]] and a.refcount(x[0]) == 2 and a.free_count() == 0

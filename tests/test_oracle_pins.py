@@ -366,3 +366,47 @@ def test_split_partials_merge_to_unsplit(oracle_mod, cuts):
         accs = np.stack([p[2] for p in parts])
         merged = oracle_mod.lse_merge(ms, ls, accs)
         np.testing.assert_allclose(merged, full[0, h], rtol=0, atol=1e-13)
+
+
+def _marked_pools(n_layers, n_blocks, block_size, heads, dim):
+    """Pools whose every (layer, block, K/V) image holds one distinct fp16
+    bit pattern, so an image's origin can be read off its contents."""
+    k = np.zeros((n_layers, n_blocks, block_size, heads, dim), dtype=np.uint16)
+    v = np.zeros_like(k)
+    for layer in range(n_layers):
+        for b in range(n_blocks):
+            k[layer, b] = 0x1000 + 64 * layer + 2 * b
+            v[layer, b] = 0x1000 + 64 * layer + 2 * b + 1
+    return k.view(np.float16), v.view(np.float16)
+
+
+def test_block_copies_move_whole_images_and_nothing_else(oracle_mod):
+    # PagedAttention blog, "Copy-on-Write for Parallel Sampling": the new
+    # block receives the shared block's contents; other blocks are untouched.
+    k, v = _marked_pools(3, 10, 16, 2, 8)
+    k0, v0 = k.copy(), v.copy()
+    oracle_mod.copy_blocks(k, v, [4, 7], [9, 1])
+    for layer in range(3):
+        assert np.array_equal(k[layer, 9], k0[layer, 4]) and np.array_equal(v[layer, 9], v0[layer, 4])
+        assert np.array_equal(k[layer, 1], k0[layer, 7]) and np.array_equal(v[layer, 1], v0[layer, 7])
+    untouched = [b for b in range(10) if b not in (9, 1)]
+    assert np.array_equal(k[:, untouched], k0[:, untouched]) and np.array_equal(v[:, untouched], v0[:, untouched])
+
+
+def test_swap_images_layout_and_round_trip(oracle_mod):
+    # Same blog, "Preemption and Swapping": blocks go to host memory one by
+    # one and come back later, possibly into other physical blocks.
+    k, v = _marked_pools(3, 10, 16, 2, 8)
+    ids = [6, 0, 3]
+    img = oracle_mod.swap_out(k, v, ids).view(np.uint16)
+    assert img.shape == (3, 3, 2, 16, 2, 8)
+    for i, b in enumerate(ids):
+        for layer in range(3):
+            assert np.all(img[i, layer, 0] == 0x1000 + 64 * layer + 2 * b)       # K
+            assert np.all(img[i, layer, 1] == 0x1000 + 64 * layer + 2 * b + 1)   # V
+    k2, v2 = np.zeros_like(k), np.zeros_like(v)
+    oracle_mod.swap_in(k2, v2, img.view(np.float16), [2, 8, 5])
+    for src, dst in zip(ids, [2, 8, 5]):
+        assert np.array_equal(k2[:, dst], k[:, src]) and np.array_equal(v2[:, dst], v[:, src])
+    others = [b for b in range(10) if b not in (2, 8, 5)]
+    assert not k2[:, others].view(np.uint16).any() and not v2[:, others].view(np.uint16).any()
