@@ -113,10 +113,36 @@ PF_API int pf_alloc_destroy(pf_alloc *a);
 /* Pop n block ids into ids_out[0..n).  All-or-nothing: PF_ERR_OOM and no
  * change if fewer than n are free (PageFault README "Test"). */
 PF_API int pf_alloc_blocks(pf_alloc *a, int n, int32_t *ids_out);
-/* Push n ids back (ids[0] first, so ids[n-1] is handed out next).  Every id
- * is checked first: one that is out of range, not allocated, or repeated in
- * the list gives PF_ERR_DOUBLE_FREE and no change. */
+/* Drop one reference per listed id; a block whose last reference goes is
+ * pushed back, in list order (ids[0] first, so the last one pushed is handed
+ * out next).  Every id is checked first: one that is out of range, free, or
+ * listed more often than it is referenced gives PF_ERR_DOUBLE_FREE and no
+ * change.  An unshared block has one reference, so this is a plain free. */
 PF_API int pf_free_blocks(pf_alloc *a, const int32_t *ids, int n);
+/* Shared blocks (PagedAttention blog, "Copy-on-Write for Parallel
+ * Sampling": sequences that share a prefix point at the same physical
+ * blocks, and a reference count tracks the sharing).  Add one reference to
+ * each listed block; all-or-nothing, PF_ERR_INVALID if one is free or out of
+ * range. */
+PF_API int pf_alloc_share(pf_alloc *a, const int32_t *ids, int n);
+/* References of block id (0 = free), or -1 for a null handle or bad id. */
+PF_API int pf_alloc_refcount(const pf_alloc *a, int32_t id);
+/* Copy-on-write, before a write into the block *entry (one host table
+ * entry): if that block has other references, pop a fresh block, move one
+ * reference to it, store it in *entry and return *src_out = old block,
+ * *dst_out = new block -- the caller copies the contents with
+ * pf_copy_blocks before writing (same section: allocate a new block, copy,
+ * update only that sequence's table).  A block with one reference is the
+ * writer's own: *src_out = *entry, *dst_out = -1, nothing changes.
+ * PF_ERR_OOM (no change) if no block is free; PF_ERR_INVALID if *entry is
+ * free or out of range. */
+PF_API int pf_alloc_cow(pf_alloc *a, int32_t *entry, int32_t *src_out, int32_t *dst_out);
+/* Fork a sequence (same section: parent and child share pages until one
+ * writes): child_row[0..ceil(len/B)) = parent_row's entries, each with one
+ * more reference.  Host int32 rows; PF_ERR_INVALID if the child row
+ * (max_blocks entries) is too short. */
+PF_API int pf_seq_fork(pf_alloc *a, int block_size, const int32_t *parent_row,
+                       int len, int32_t *child_row, int max_blocks);
 /* Number of free blocks, or -1 for a null handle. */
 PF_API int pf_alloc_free_count(const pf_alloc *a);
 /* Demand paging (PagedAttention blog, "Architecture"): grow one sequence
@@ -159,6 +185,34 @@ PF_API int pf_gather_kv(const pf_pool *pool, int layer, const int32_t *block_tab
                  int max_blocks_per_seq, const int32_t *context_lens,
                  const int64_t *cu_off, int n_seqs, void *k_out, void *v_out,
                  void *stream);
+
+/* ------------------------------------------- whole-block copies ---- */
+
+/* Bytes of one block image: block b's K then V rows of layer 0, then of
+ * layer 1, ...: [n_layers][2][B][Hkv][D] fp16.  0 for a null pool. */
+PF_API size_t pf_block_image_bytes(const pf_pool *pool);
+/* Copy-on-write copies (PagedAttention blog, "Copy-on-Write for Parallel
+ * Sampling"): for i < n, block dst_ids[i] takes the contents of block
+ * src_ids[i] in every layer, K and V.  src_ids, dst_ids: device int32 [n].
+ * A destination must not also be a source or another pair's destination.
+ * Ids outside [0, n_blocks) set PF_DEV_BAD_BLOCK_ID and that pair is
+ * skipped.  Bit-exact.  n == 0 is a no-op. */
+PF_API int pf_copy_blocks(const pf_pool *pool, const int32_t *src_ids,
+                          const int32_t *dst_ids, int n, void *stream);
+/* Swap out (same blog, "Preemption and Swapping": under memory pressure a
+ * sequence's blocks are evicted to CPU memory, per block): the images of
+ * blocks ids[0..n) (device int32) are written to host_dst[i] (n images of
+ * pf_block_image_bytes each).  host_dst must be page-locked host memory
+ * (cudaHostAlloc, cudaHostRegister, a pinned torch tensor); the kernel
+ * writes it directly through its device mapping, with no staging copy.
+ * PF_ERR_INVALID otherwise.  Bad ids are flagged and skipped as above. */
+PF_API int pf_swap_out(const pf_pool *pool, const int32_t *ids, int n,
+                       void *host_dst, void *stream);
+/* Swap in: blocks ids[0..n) take the contents of the host images
+ * host_src[0..n) (page-locked, as above; any block ids, so a sequence can
+ * come back into other physical blocks -- patch its table to match). */
+PF_API int pf_swap_in(const pf_pool *pool, const void *host_src,
+                      const int32_t *ids, int n, void *stream);
 
 /* Workspace bytes pf_paged_decode_attention needs for a batch of n_seqs
  * sequences of at most max_blocks_per_seq * block_size tokens with

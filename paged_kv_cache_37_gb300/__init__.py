@@ -14,7 +14,9 @@ from ._native import (  # noqa: F401
     PF_F16, PF_F32, PF_OK,
     Allocator, DoubleFree, OutOfBlocks, PagedKVError, Pool,
     build, lib,
-    pf_abi_version, pf_alloc_blocks, pf_alloc_create, pf_alloc_destroy, pf_alloc_free_count,
+    pf_abi_version, pf_alloc_blocks, pf_alloc_cow, pf_alloc_create, pf_alloc_destroy, pf_alloc_free_count,
+    pf_alloc_refcount, pf_alloc_share, pf_block_image_bytes, pf_copy_blocks, pf_seq_fork, pf_swap_in,
+    pf_swap_out,
     pf_decode_step, pf_decode_workspace_bytes, pf_decode_workspace_init, pf_device_status, pf_free_blocks,
     pf_gather_kv, pf_last_error, pf_paged_decode_attention, pf_paged_decode_attention_noalloc,
     pf_pool_bytes, pf_pool_create,

@@ -75,6 +75,14 @@ def lib():
         "pf_alloc_free_count": (I, [P]),
         "pf_seq_reserve": (I, [P, I, P, I, I, I]),
         "pf_seq_release": (I, [P, I, P, I]),
+        "pf_alloc_share": (I, [P, P, I]),
+        "pf_alloc_refcount": (I, [P, ctypes.c_int32]),
+        "pf_alloc_cow": (I, [P, P, P, P]),
+        "pf_seq_fork": (I, [P, I, P, I, P, I]),
+        "pf_block_image_bytes": (Z, [P]),
+        "pf_copy_blocks": (I, [P, P, P, I, P]),
+        "pf_swap_out": (I, [P, P, I, P, P]),
+        "pf_swap_in": (I, [P, P, P, I, P]),
         "pf_write_kv": (I, [P, I, P, P, P, I, I, P, P, I, P]),
         "pf_gather_kv": (I, [P, I, P, I, P, P, I, P, P, P]),
         "pf_decode_workspace_bytes": (Z, [P, I, I, I, I]),
@@ -228,6 +236,76 @@ def pf_seq_reserve(alloc, block_size, table_row, cur_len, new_len):
 
 def pf_seq_release(alloc, block_size, table_row, length):
     _check(lib().pf_seq_release(alloc.handle, block_size, _host_i32(table_row, "table_row"), length))
+
+
+def pf_alloc_share(alloc, ids):
+    """One more reference on each listed block (a fork's shared prefix)."""
+    import numpy as np
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    _check(lib().pf_alloc_share(alloc.handle, ids.ctypes.data_as(ctypes.c_void_p), ids.size))
+
+
+def pf_alloc_refcount(alloc, block):
+    return lib().pf_alloc_refcount(alloc.handle, int(block))
+
+
+def pf_alloc_cow(alloc, table_row, j):
+    """Copy-on-write of table_row[j] (host int32 numpy row, patched in place)
+    before a write into that block.  Returns None when the block is the
+    writer's own, else (old block, new block) for pf_copy_blocks."""
+    import numpy as np
+    if not isinstance(table_row, np.ndarray) or table_row.dtype != np.int32:
+        raise TypeError("table_row must be a numpy int32 array")
+    entry = table_row[j:j + 1]
+    src, dst = ctypes.c_int32(), ctypes.c_int32()
+    _check(lib().pf_alloc_cow(alloc.handle, entry.ctypes.data_as(ctypes.c_void_p), ctypes.byref(src),
+                              ctypes.byref(dst)))
+    return None if dst.value < 0 else (src.value, dst.value)
+
+
+def pf_seq_fork(alloc, block_size, parent_row, length, child_row):
+    """child_row[:ceil(length/B)] = parent_row's blocks, shared (host int32 rows)."""
+    _check(lib().pf_seq_fork(alloc.handle, block_size, _host_i32(parent_row, "parent_row"), length,
+                             _host_i32(child_row, "child_row"), child_row.size))
+
+
+def pf_block_image_bytes(pool):
+    return lib().pf_block_image_bytes(pool.handle)
+
+
+def pf_copy_blocks(pool, src_ids, dst_ids, stream=None):
+    """Block dst_ids[i] := block src_ids[i], every layer, K and V (device int32)."""
+    import torch
+    n = src_ids.numel()
+    if dst_ids.numel() != n:
+        raise PagedKVError(PF_ERR_INVALID, "src_ids and dst_ids must have the same length")
+    _check(lib().pf_copy_blocks(pool.handle, _dev_ptr(src_ids, "src_ids", torch.int32),
+                                _dev_ptr(dst_ids, "dst_ids", torch.int32), n, _stream_ptr(stream)))
+
+
+def _pinned_ptr(t, name, nbytes):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned() or not t.is_contiguous():
+        raise PagedKVError(PF_ERR_INVALID, f"{name} must be a contiguous pinned host tensor")
+    if t.numel() * t.element_size() < nbytes:
+        raise PagedKVError(PF_ERR_INVALID, f"{name} holds {t.numel() * t.element_size()} bytes, needs {nbytes}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def pf_swap_out(pool, ids, host_dst, stream=None):
+    """Images of blocks ids (device int32) into the pinned host tensor host_dst."""
+    import torch
+    n = ids.numel()
+    ptr = _pinned_ptr(host_dst, "host_dst", n * pf_block_image_bytes(pool))
+    _check(lib().pf_swap_out(pool.handle, _dev_ptr(ids, "ids", torch.int32), n, ptr, _stream_ptr(stream)))
+
+
+def pf_swap_in(pool, host_src, ids, stream=None):
+    """Blocks ids (device int32) take the images in the pinned host tensor host_src."""
+    import torch
+    n = ids.numel()
+    ptr = _pinned_ptr(host_src, "host_src", n * pf_block_image_bytes(pool))
+    _check(lib().pf_swap_in(pool.handle, ptr, _dev_ptr(ids, "ids", torch.int32), n, _stream_ptr(stream)))
 
 
 def pf_write_kv(pool, layer, k_new, v_new, block_tables, seq_idx, pos, stream=None):

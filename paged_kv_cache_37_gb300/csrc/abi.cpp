@@ -141,6 +141,65 @@ int pf_gather_kv(const pf_pool *pool, int layer, const int32_t *block_tables, in
     return pkv::launch_gather_kv(a, static_cast<cudaStream_t>(stream));
 }
 
+size_t pf_block_image_bytes(const pf_pool *pool) {
+    if (!pool) return 0;
+    return (size_t)pool->n_layers * 2 * pool->block_size * pool->n_kv_heads * pool->head_dim * sizeof(uint16_t);
+}
+
+int pf_copy_blocks(const pf_pool *pool, const int32_t *src_ids, const int32_t *dst_ids, int n, void *stream) {
+    pkv::clear_error();
+    if (!pool) return pkv::set_error(PF_ERR_INVALID, "pf_copy_blocks: pool is null");
+    if (n < 0) return pkv::set_error(PF_ERR_INVALID, "pf_copy_blocks: negative count");
+    if (n == 0) return PF_OK;
+    if (!src_ids || !dst_ids) return pkv::set_error(PF_ERR_INVALID, "pf_copy_blocks: null id array");
+    pkv::BlockCopyArgs a{pool, src_ids, dst_ids, nullptr, n};
+    return pkv::launch_block_copy(a, static_cast<cudaStream_t>(stream));
+}
+
+// Device address of a page-locked host buffer (its mapping), or an error.
+static int host_image_ptr(const void *host, void **dev_out, const char *what) {
+    if (!host) return pkv::set_error(PF_ERR_INVALID, std::string(what) + ": host buffer is null");
+    if (!aligned16(host)) return pkv::set_error(PF_ERR_INVALID, std::string(what) + ": host buffer must be 16-byte aligned");
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, host);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return pkv::cuda_error(e, (std::string(what) + ": cudaPointerGetAttributes").c_str());
+    }
+    if (attr.type != cudaMemoryTypeHost || attr.devicePointer == nullptr)
+        return pkv::set_error(PF_ERR_INVALID, std::string(what) +
+                                                  ": host buffer must be page-locked host memory "
+                                                  "(cudaHostAlloc, cudaHostRegister or a pinned tensor)");
+    *dev_out = attr.devicePointer;
+    return PF_OK;
+}
+
+int pf_swap_out(const pf_pool *pool, const int32_t *ids, int n, void *host_dst, void *stream) {
+    pkv::clear_error();
+    if (!pool) return pkv::set_error(PF_ERR_INVALID, "pf_swap_out: pool is null");
+    if (n < 0) return pkv::set_error(PF_ERR_INVALID, "pf_swap_out: negative count");
+    if (n == 0) return PF_OK;
+    if (!ids) return pkv::set_error(PF_ERR_INVALID, "pf_swap_out: ids is null");
+    void *img = nullptr;
+    int rc = host_image_ptr(host_dst, &img, "pf_swap_out");
+    if (rc) return rc;
+    pkv::BlockCopyArgs a{pool, ids, nullptr, img, n};
+    return pkv::launch_block_copy(a, static_cast<cudaStream_t>(stream));
+}
+
+int pf_swap_in(const pf_pool *pool, const void *host_src, const int32_t *ids, int n, void *stream) {
+    pkv::clear_error();
+    if (!pool) return pkv::set_error(PF_ERR_INVALID, "pf_swap_in: pool is null");
+    if (n < 0) return pkv::set_error(PF_ERR_INVALID, "pf_swap_in: negative count");
+    if (n == 0) return PF_OK;
+    if (!ids) return pkv::set_error(PF_ERR_INVALID, "pf_swap_in: ids is null");
+    void *img = nullptr;
+    int rc = host_image_ptr(host_src, &img, "pf_swap_in");
+    if (rc) return rc;
+    pkv::BlockCopyArgs a{pool, nullptr, ids, img, n};
+    return pkv::launch_block_copy(a, static_cast<cudaStream_t>(stream));
+}
+
 size_t pf_decode_workspace_bytes(const pf_pool *pool, int n_seqs, int n_q_heads, int max_blocks_per_seq,
                                  int split_tokens) {
     pkv::clear_error();

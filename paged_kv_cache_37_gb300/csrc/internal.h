@@ -70,6 +70,18 @@ struct WriteArgs {
 };
 int launch_write_kv(const WriteArgs &a, cudaStream_t stream);
 
+// Whole-block copies: pool -> pool (both id arrays set), pool -> image
+// (dst_ids null: destination i is image i of `image`), image -> pool
+// (src_ids null).  Ids are device int32 arrays of n entries.
+struct BlockCopyArgs {
+    const pf_pool *pool;
+    const int32_t *src_ids;
+    const int32_t *dst_ids;
+    const void *image;   // device-accessible address of the host images
+    int n;
+};
+int launch_block_copy(const BlockCopyArgs &a, cudaStream_t stream);
+
 struct GatherArgs {
     const pf_pool *pool;
     int layer;

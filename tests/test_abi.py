@@ -98,6 +98,18 @@ def test_device_calls_reject_bad_arguments_before_launch(pkv):
     assert "flags" in pkv.pf_last_error()
     assert lib.pf_decode_step(*step(flags=pkv.PF_STEP_OVERLAP_PREVIOUS | 4)) == pkv.PF_ERR_INVALID
     assert lib.pf_decode_step(*step(kn=None)) == pkv.PF_ERR_INVALID
+    # whole-block copies and swapping: null pool / ids / buffer, negative counts; 0 is a no-op
+    assert lib.pf_block_image_bytes(pool) == 1 * 2 * 16 * 12 * 64 * 2
+    assert lib.pf_block_image_bytes(None) == 0
+    assert lib.pf_copy_blocks(None, ok, ok, 1, None) == pkv.PF_ERR_INVALID
+    assert lib.pf_copy_blocks(pool, ok, None, 1, None) == pkv.PF_ERR_INVALID
+    assert lib.pf_copy_blocks(pool, ok, ok, -1, None) == pkv.PF_ERR_INVALID
+    assert lib.pf_copy_blocks(pool, None, None, 0, None) == pkv.PF_OK
+    assert lib.pf_swap_out(pool, None, 2, ok, None) == pkv.PF_ERR_INVALID
+    assert lib.pf_swap_out(pool, ok, 2, None, None) == pkv.PF_ERR_INVALID
+    assert lib.pf_swap_out(pool, ok, 2, P(0x30008), None) == pkv.PF_ERR_INVALID      # not 16-byte aligned
+    assert lib.pf_swap_in(pool, ok, ok, -3, None) == pkv.PF_ERR_INVALID
+    assert lib.pf_swap_in(pool, None, None, 0, None) == pkv.PF_OK
     lib.pf_pool_destroy(pool)
 
 

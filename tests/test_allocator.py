@@ -110,3 +110,77 @@ def test_seq_reserve_rejects_short_row_and_is_atomic_on_oom(pkv):
     assert other.tolist() == [0, 0, 0, 0] and pkv.pf_alloc_free_count(a) == 1
     with pytest.raises(pkv.PagedKVError):
         pkv.pf_seq_reserve(a, 16, row, 33, 20)     # shrinking is not a reserve
+
+
+def test_shared_blocks_and_copy_on_write_match_model(pkv):
+    """Forks, copy-on-write and frees of shared blocks: the product and the
+    model hand out the same ids and keep the same reference counts, and fail
+    on the same steps (PagedAttention blog, "Copy-on-Write for Parallel
+    Sampling")."""
+    B, N, MAXB = 16, 96, 12
+    a = pkv.pf_alloc_create(N, 5)
+    m = FreeListModel(N, 5)
+    rng = random.Random(3)
+    seqs = []   # (product row, model row, length)
+    for step in range(3000):
+        r = rng.random()
+        if r < 0.25 or not seqs:                 # new sequence
+            L = rng.randrange(1, MAXB * B)
+            row = np.zeros(MAXB, dtype=np.int32)
+            mrow = [0] * MAXB
+            try:
+                m.seq_reserve(mrow, B, 0, L)
+                ok = True
+            except ModelOOM:
+                ok = False
+            if ok:
+                pkv.pf_seq_reserve(a, B, row, 0, L)
+                seqs.append((row, mrow, L))
+            else:
+                with pytest.raises(pkv.OutOfBlocks):
+                    pkv.pf_seq_reserve(a, B, row, 0, L)
+        elif r < 0.45:                            # fork a prefix
+            row, mrow, L = seqs[rng.randrange(len(seqs))]
+            Lc = rng.randrange(1, L + 1)
+            child = np.zeros(MAXB, dtype=np.int32)
+            pkv.pf_seq_fork(a, B, row, Lc, child)
+            mchild = m.seq_fork(mrow, B, Lc) + [0] * (MAXB - -(-Lc // B))
+            seqs.append((child, mchild, Lc))
+        elif r < 0.7:                             # write into a block: copy-on-write first
+            row, mrow, L = seqs[rng.randrange(len(seqs))]
+            j = rng.randrange(-(-L // B))
+            try:
+                want = m.cow(mrow, j)
+                ok = True
+            except ModelOOM:
+                ok = False
+            if ok:
+                got = pkv.pf_alloc_cow(a, row, j)
+                assert got == want
+            else:
+                before = row.copy()
+                with pytest.raises(pkv.OutOfBlocks):
+                    pkv.pf_alloc_cow(a, row, j)
+                assert np.array_equal(row, before)
+        else:                                     # a sequence finishes
+            row, mrow, L = seqs.pop(rng.randrange(len(seqs)))
+            pkv.pf_seq_release(a, B, row, L)
+            m.seq_release(mrow, B, L)
+        assert pkv.pf_alloc_free_count(a) == m.free_count()
+        if step % 97 == 0:
+            assert [pkv.pf_alloc_refcount(a, b) for b in range(N)] == [m.refcount(b) for b in range(N)]
+        for row, mrow, L in seqs[-3:]:
+            assert row.tolist() == mrow
+    # a block listed more often than it is referenced: error, no change
+    for row, mrow, L in seqs:
+        pkv.pf_seq_release(a, B, row, L)
+        m.seq_release(mrow, B, L)
+    assert pkv.pf_alloc_free_count(a) == N == m.free_count()
+    ids = pkv.pf_alloc_blocks(a, 2)
+    pkv.pf_alloc_share(a, ids[:1])
+    with pytest.raises(pkv.DoubleFree):
+        pkv.pf_free_blocks(a, [ids[0], ids[0], ids[0]])
+    assert pkv.pf_alloc_refcount(a, ids[0]) == 2
+    with pytest.raises(pkv.PagedKVError):
+        pkv.pf_alloc_share(a, [N - 1 if N - 1 not in ids else 0])   # a free block
+    assert pkv.pf_alloc_refcount(a, -1) == -1
