@@ -216,6 +216,28 @@ def attention_paged(q, k_pool, v_pool, layer, block_tables, context_lens, scale)
     return out
 
 
+def prefill_attention(q, k_pool, v_pool, layer, block_tables, context_lens, cu_q, scale):
+    """Multi-token append (a prompt, or a chunk of one, written into the
+    sequence's last pages: PagedAttention blog, "Architecture", append then
+    attend).  Sequence s's new tokens are q rows cu_q[s] .. cu_q[s + 1] - 1,
+    its last n_s = cu_q[s + 1] - cu_q[s] positions of L_s = context_lens[s];
+    the query at position p = L_s - n_s + i attends causally to tokens
+    0 .. p, which is single-query attention over those p + 1 tokens.
+    q [T_q, Hq, D] fp16 -> fp64 [T_q, Hq, D]."""
+    bt = _i32(block_tables)
+    lens = _i32(context_lens)
+    cu = np.asarray(cu_q, dtype=np.int64)
+    rows, qlen = [], []
+    for s in range(lens.size):
+        n = int(cu[s + 1] - cu[s])
+        for i in range(n):
+            rows.append(s)
+            qlen.append(int(lens[s]) - n + i + 1)
+    if not rows:
+        return np.zeros((0,) + tuple(q.shape[1:]), dtype=np.float64)
+    return attention_paged(q, k_pool, v_pool, layer, bt[np.asarray(rows)], np.asarray(qlen, dtype=np.int32), scale)
+
+
 def attention_partial(q_row, k, v, head, t0, t1, scale):
     """Partial (m, l, acc) of one query row over tokens [t0, t1) of a contiguous
     sequence k/v [L, Hkv, D]."""

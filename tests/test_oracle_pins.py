@@ -410,3 +410,52 @@ def test_swap_images_layout_and_round_trip(oracle_mod):
         assert np.array_equal(k2[:, dst], k[:, src]) and np.array_equal(v2[:, dst], v[:, src])
     others = [b for b in range(10) if b not in (2, 8, 5)]
     assert not k2[:, others].view(np.uint16).any() and not v2[:, others].view(np.uint16).any()
+
+
+def _prompt_pool(tokens, heads, dim, seed):
+    """One-layer pool holding a `tokens`-token prompt in shuffled 16-token
+    pages, plus its table row."""
+    B = 16
+    n_pages = -(-tokens // B)
+    table = np.array(np.random.default_rng(seed).permutation(n_pages + 3)[:n_pages], dtype=np.int32)
+    k = si.fp16_normal((1, n_pages + 3, B, heads, dim), seed + 1)
+    v = si.fp16_normal((1, n_pages + 3, B, heads, dim), seed + 2)
+    return k, v, table[None, :]
+
+
+def test_prefill_of_a_two_token_prompt_closed_form(oracle_mod):
+    # Prompt of two tokens, both new: query 0 sees token 0 only (its output
+    # is V0 exactly); query 1 sees both (the two-term softmax).
+    heads, dim, scale = 3, 64, 0.125
+    k, v, bt = _prompt_pool(2, heads, dim, 31)
+    q = si.fp16_normal((2, heads, dim), 34)
+    out = oracle_mod.prefill_attention(q, k, v, 0, bt, [2], [0, 2], scale)
+    K = k.astype(np.float64)[0][bt[0]].reshape(-1, heads, dim)
+    V = v.astype(np.float64)[0][bt[0]].reshape(-1, heads, dim)
+    Q = q.astype(np.float64)
+    for h in range(heads):
+        assert np.array_equal(out[0, h], V[0, h])
+        z0 = scale * Q[1, h] @ K[0, h]
+        z1 = scale * Q[1, h] @ K[1, h]
+        w0 = 1.0 / (1.0 + math.exp(z1 - z0))
+        assert np.allclose(out[1, h], w0 * V[0, h] + (1.0 - w0) * V[1, h], rtol=0, atol=1e-12)
+
+
+def test_prefill_is_causal(oracle_mod):
+    # A later token's keys and values never reach an earlier query; an
+    # earlier token's do.
+    heads, dim, L, n = 2, 64, 40, 6
+    k, v, bt = _prompt_pool(L, heads, dim, 41)
+    q = si.fp16_normal((n, heads, dim), 44)
+    base = oracle_mod.prefill_attention(q, k, v, 0, bt, [L], [0, n], 0.125)
+    page, off = divmod(L - 1, 16)              # the last token, position L - 1
+    k2 = k.copy()
+    k2[0, bt[0, page], off] = np.float16(7.0)
+    out = oracle_mod.prefill_attention(q, k2, v, 0, bt, [L], [0, n], 0.125)
+    assert np.array_equal(out[: n - 1], base[: n - 1])      # queries at L - 6 .. L - 2
+    assert not np.array_equal(out[n - 1], base[n - 1])      # the query at L - 1 sees it
+    page, off = divmod(L - n, 16)               # the first new token
+    k3 = k.copy()
+    k3[0, bt[0, page], off] = np.float16(7.0)
+    out = oracle_mod.prefill_attention(q, k3, v, 0, bt, [L], [0, n], 0.125)
+    assert all(not np.array_equal(out[i], base[i]) for i in range(n))
