@@ -423,7 +423,68 @@ def run_ours(args, dist):
     g_bytes = gather_bytes(lens, Hkv, D, B)
     del outs
 
+    # whole-block legs: copy-on-write copies inside a pool (half the pool's
+    # blocks onto the other half) and swapping the same blocks out to pinned
+    # host memory and back in; bytes = every image read once and written once
+    img = pkv.pf_block_image_bytes(reps[0]["pool"])
+    nb = w["n_blocks"] // 2
+    src_ids = to(np.arange(nb, dtype=np.int32))
+    dst_ids = to(np.arange(nb, 2 * nb, dtype=np.int32))
+    blk_bytes = 2 * nb * img
+    swap_buf = torch.empty(nb * img, dtype=torch.uint8).pin_memory()
+
+    def time_calls(fn, n):
+        for i in range(3):
+            fn(i)
+        dist.barrier()
+        torch.cuda.synchronize(device)
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for i in range(n):
+            fn(i)
+        b1.record(stream)
+        torch.cuda.synchronize(device)
+        return dist.max(b0.elapsed_time(b1) / n)
+
+    copy_ms = time_calls(lambda i: check(lib.pf_copy_blocks(reps[i % R]["pool"].handle, P(src_ids), P(dst_ids),
+                                                             nb, sp)), Kg)
+    swap_out_ms = time_calls(lambda i: check(lib.pf_swap_out(reps[i % R]["pool"].handle, P(src_ids), nb,
+                                                              P(swap_buf), sp)), 10)
+    swap_in_ms = time_calls(lambda i: check(lib.pf_swap_in(reps[i % R]["pool"].handle, P(swap_buf), P(dst_ids),
+                                                            nb, sp)), 10)
+    # the platform's own rate for the same bytes: copy-engine copies between
+    # device memory and the same pinned buffer
+    ce_dev = torch.empty(nb * img, dtype=torch.uint8, device=device)
+    ce_d2h_ms = time_calls(lambda i: swap_buf.copy_(ce_dev, non_blocking=True), 10)
+    ce_h2d_ms = time_calls(lambda i: ce_dev.copy_(swap_buf, non_blocking=True), 10)
+    del swap_buf, ce_dev
+
+    # multi-token append legs.  (1) 8 new tokens at the end of every sequence
+    # of the workload (each sequence's K/V read once per kv-head: HBM-bound);
+    # (2) whole prompts, 4 x 2048 tokens (causal attention over each prompt:
+    # fp32 FMA-bound on the CUDA cores)
+    n_app = 8
+    cu_app = to(np.arange(S + 1, dtype=np.int32) * n_app)
+    q_app = torch.randn((S * n_app, Hq, D), device=device).half()
+    o_app = torch.empty_like(q_app)
+    app_args = [(reps[r]["pool"].handle, 0, P(q_app), P(tables["shuffled"]), maxb, P(lens_d), P(cu_app), S, n_app,
+                 Hq, ctypes.c_float(w["scale"]), P(o_app), pkv.PF_F16, sp) for r in range(R)]
+    app_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*app_args[i % R])), Kg)
+    app_bytes = attention_bytes(lens, Hq, Hkv, D, B) + (n_app - 1) * S * Hq * D * 2 * 2 + 4 * (S + 1)
+    Lp, Sp = 2048, 4
+    pr_lens = to(np.full(Sp, Lp, dtype=np.int32))
+    pr_bt = to(np.arange(Sp * Lp // B, dtype=np.int32).reshape(Sp, Lp // B))
+    pr_cu = to(np.arange(Sp + 1, dtype=np.int32) * Lp)
+    q_pr = torch.randn((Sp * Lp, Hq, D), device=device).half()
+    o_pr = torch.empty_like(q_pr)
+    pr_args = (reps[0]["pool"].handle, 0, P(q_pr), P(pr_bt), Lp // B, P(pr_lens), P(pr_cu), Sp, Lp, Hq,
+               ctypes.c_float(w["scale"]), P(o_pr), pkv.PF_F16, sp)
+    pr_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*pr_args)), 10)
+    pr_flops = 4.0 * Hq * D * Sp * Lp * (Lp + 1) / 2        # q.k and p.v over every causal pair
+    del q_app, o_app, q_pr, o_pr
+
     clocks = sampler.stop()
+    fp32_peak = props.multi_processor_count * 128 * 2 * (clocks.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
     status = pkv.pf_device_status(reset=True)
     if status:
         raise RuntimeError(f"device status word {status} after the timed runs")
@@ -500,6 +561,25 @@ def run_ours(args, dist):
         "ordered": {"ms_per_step": round(ms_ord / K, 5), "decode_step_ms": round(step_ord_ms, 5),
                     "gbs": round(step_bytes / (step_ord_ms / 1e3) / 1e9, 1),
                     "shuffled_over_ordered_time": round(step_call_ms / step_ord_ms, 4)},
+        "block_copies": {"blocks": nb, "bytes": blk_bytes, "image_bytes": img,
+                         "copy_gbs": round(blk_bytes / (copy_ms / 1e3) / 1e9, 1), "copy_ms": round(copy_ms, 5),
+                         "copy_frac_of_measured_copy": round(blk_bytes / (copy_ms / 1e3) / 1e9 / peak, 4),
+                         "swap_out_gbs": round(blk_bytes / 2 / (swap_out_ms / 1e3) / 1e9, 1),
+                         "swap_in_gbs": round(blk_bytes / 2 / (swap_in_ms / 1e3) / 1e9, 1),
+                         "copy_engine_d2h_gbs": round(blk_bytes / 2 / (ce_d2h_ms / 1e3) / 1e9, 1),
+                         "copy_engine_h2d_gbs": round(blk_bytes / 2 / (ce_h2d_ms / 1e3) / 1e9, 1),
+                         "swap_out_frac_of_copy_engine": round(ce_d2h_ms / swap_out_ms, 4),
+                         "swap_in_frac_of_copy_engine": round(ce_h2d_ms / swap_in_ms, 4),
+                         "swap_note": "GB/s of images moved between HBM and page-locked host memory; the "
+                                      "copy engine's rate for the same bytes and buffer is the roofline"},
+        "append_attention": {"new_tokens_per_seq": n_app, "ms": round(app_ms, 5), "bytes": app_bytes,
+                             "gbs": round(app_bytes / (app_ms / 1e3) / 1e9, 1),
+                             "frac_of_measured_copy": round(app_bytes / (app_ms / 1e3) / 1e9 / peak, 4)},
+        "prompt_prefill": {"prompts": Sp, "tokens": Lp, "ms": round(pr_ms, 4), "flops": pr_flops,
+                           "tflops": round(pr_flops / (pr_ms / 1e3) / 1e12, 2), "bound": "alu",
+                           "fp32_fma_peak_tflops": round(fp32_peak, 1),
+                           "frac": round(pr_flops / (pr_ms / 1e3) / 1e12 / fp32_peak, 4),
+                           "peak_note": "SMs x 128 fp32 lanes x 2 flop x max SM clock (CUDA cores, no tensor cores)"},
         "gather": {"gbs": round(g_bytes / (gather_ms / 1e3) / 1e9, 1), "ms": round(gather_ms, 5),
                    "bytes": g_bytes, "frac_of_measured_copy": round(g_bytes / (gather_ms / 1e3) / 1e9 / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

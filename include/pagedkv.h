@@ -284,6 +284,31 @@ PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
                           int out_dtype, int split_tokens, void *workspace,
                           size_t ws_bytes, int flags, void *stream);
 
+/* Multi-token append attention: a prompt, or a chunk of one, whose K/V rows
+ * were already written into the sequence's last pages (pf_write_kv), then
+ * attended to (PagedAttention blog, "Architecture": append, then attend;
+ * PageFault README, "Four stages": the prompt is reserved up front).
+ * Sequence s has L = context_lens[s] tokens, the last n_s = cu_q[s + 1] -
+ * cu_q[s] of them new; their queries are rows cu_q[s] .. cu_q[s + 1] - 1 of
+ * q (fp16 [T_q][n_q_heads][D], T_q = cu_q[n_seqs]).  The query of new token
+ * i sits at position p = L - n_s + i and attends causally to tokens 0 .. p:
+ *   out[row][hq][d] = sum_{t <= p} softmax_t(scale * q . K[slot(s, t)][h]) V[..][h][d]
+ * with h = hq / (n_q_heads / Hkv); fp32 accumulation; out has q's shape, of
+ * out_dtype.  A decode step is the case n_s = 1.  cu_q: device int32
+ * [n_seqs + 1], non-decreasing; max_new_tokens bounds every n_s (it sizes
+ * the grid).  On the device, n_s > L or > max_new_tokens, or a length
+ * outside the table, sets PF_DEV_BAD_LENGTH and is clamped; bad block ids set
+ * PF_DEV_BAD_BLOCK_ID.  No workspace. */
+PF_API int pf_paged_prefill_attention(const pf_pool *pool, int layer,
+                                      const void *q,
+                                      const int32_t *block_tables,
+                                      int max_blocks_per_seq,
+                                      const int32_t *context_lens,
+                                      const int32_t *cu_q, int n_seqs,
+                                      int max_new_tokens, int n_q_heads,
+                                      float scale, void *out, int out_dtype,
+                                      void *stream);
+
 /* The decode attention call for callers that cannot allocate device memory.
  * No counterpart on the pages: it exists for code that may only touch the
  * buffers it is handed -- for instance an operator inside another runtime

@@ -19,6 +19,7 @@ from ._native import (  # noqa: F401
     pf_swap_out,
     pf_decode_step, pf_decode_workspace_bytes, pf_decode_workspace_init, pf_device_status, pf_free_blocks,
     pf_gather_kv, pf_last_error, pf_paged_decode_attention, pf_paged_decode_attention_noalloc,
+    pf_paged_prefill_attention,
     pf_pool_bytes, pf_pool_create,
     pf_pool_destroy, pf_seq_release, pf_seq_reserve, pf_write_kv,
 )

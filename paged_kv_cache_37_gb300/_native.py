@@ -80,6 +80,7 @@ def lib():
         "pf_alloc_cow": (I, [P, P, P, P]),
         "pf_seq_fork": (I, [P, I, P, I, P, I]),
         "pf_block_image_bytes": (Z, [P]),
+        "pf_paged_prefill_attention": (I, [P, I, P, P, I, P, P, I, I, I, F, P, I, P]),
         "pf_copy_blocks": (I, [P, P, P, I, P]),
         "pf_swap_out": (I, [P, P, I, P, P]),
         "pf_swap_in": (I, [P, P, P, I, P]),
@@ -306,6 +307,26 @@ def pf_swap_in(pool, host_src, ids, stream=None):
     n = ids.numel()
     ptr = _pinned_ptr(host_src, "host_src", n * pf_block_image_bytes(pool))
     _check(lib().pf_swap_in(pool.handle, ptr, _dev_ptr(ids, "ids", torch.int32), n, _stream_ptr(stream)))
+
+
+def pf_paged_prefill_attention(pool, layer, q, block_tables, context_lens, cu_q, max_new_tokens, scale, out,
+                               stream=None):
+    """Causal attention of each sequence's last n_s = cu_q[s+1] - cu_q[s]
+    tokens (q rows cu_q[s]..cu_q[s+1]-1) over its context (device tensors)."""
+    import torch
+    n = context_lens.numel()
+    if block_tables.dim() != 2 or block_tables.shape[0] != n or cu_q.numel() != n + 1:
+        raise PagedKVError(PF_ERR_INVALID, "block_tables must be [n_seqs, max_blocks]; cu_q [n_seqs + 1]")
+    if tuple(out.shape) != tuple(q.shape):
+        raise PagedKVError(PF_ERR_INVALID, "out must have the shape of q")
+    out_dtype = {torch.float16: PF_F16, torch.float32: PF_F32}.get(out.dtype)
+    if out_dtype is None:
+        raise PagedKVError(PF_ERR_INVALID, "out must be float16 or float32")
+    _check(lib().pf_paged_prefill_attention(
+        pool.handle, layer, _dev_ptr(q, "q", torch.float16), _dev_ptr(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32),
+        _dev_ptr(cu_q, "cu_q", torch.int32), n, int(max_new_tokens), q.shape[1], float(scale),
+        _dev_ptr(out, "out"), out_dtype, _stream_ptr(stream)))
 
 
 def pf_write_kv(pool, layer, k_new, v_new, block_tables, seq_idx, pos, stream=None):

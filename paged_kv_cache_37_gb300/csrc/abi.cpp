@@ -298,6 +298,36 @@ int pf_decode_step(const pf_pool *pool, int layer, const void *q, const void *k_
                        n_q_heads, scale, out, out_dtype, split_tokens, workspace, ws_bytes, stream);
 }
 
+int pf_paged_prefill_attention(const pf_pool *pool, int layer, const void *q, const int32_t *block_tables,
+                               int max_blocks_per_seq, const int32_t *context_lens, const int32_t *cu_q, int n_seqs,
+                               int max_new_tokens, int n_q_heads, float scale, void *out, int out_dtype,
+                               void *stream) {
+    pkv::clear_error();
+    int rc = check_pool(pool, layer, "pf_paged_prefill_attention");
+    if (rc) return rc;
+    if (n_seqs < 0 || max_new_tokens < 0)
+        return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: negative n_seqs or max_new_tokens");
+    if (n_seqs == 0 || max_new_tokens == 0) return PF_OK;
+    if (!q || !block_tables || !context_lens || !cu_q || !out)
+        return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: null pointer");
+    if (!aligned16(q) || !aligned16(out))
+        return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: q and out must be 16-byte aligned");
+    if (out_dtype != PF_F16 && out_dtype != PF_F32)
+        return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: out_dtype must be PF_F16 or PF_F32");
+    if (n_q_heads <= 0 || n_q_heads % pool->n_kv_heads)
+        return pkv::set_error(PF_ERR_INVALID,
+                              "pf_paged_prefill_attention: n_q_heads must be a positive multiple of n_kv_heads");
+    if (n_q_heads / pool->n_kv_heads > 8)
+        return pkv::set_error(PF_ERR_UNSUPPORTED, "pf_paged_prefill_attention: at most 8 q-heads per kv-head are built");
+    if (max_blocks_per_seq <= 0 || (long long)max_blocks_per_seq * pool->block_size > (1ll << 30))
+        return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: bad max_blocks_per_seq");
+    if (!(scale > 0.0f) || scale != scale)
+        return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: scale must be a positive number");
+    pkv::PrefillArgs a{pool, layer, q, block_tables, max_blocks_per_seq, context_lens, cu_q, n_seqs, max_new_tokens,
+                       n_q_heads, scale, out, out_dtype};
+    return pkv::launch_prefill(a, static_cast<cudaStream_t>(stream));
+}
+
 int pf_device_status(int *status_out, int reset, void *stream) {
     pkv::clear_error();
     if (!status_out) return pkv::set_error(PF_ERR_INVALID, "pf_device_status: status_out is null");

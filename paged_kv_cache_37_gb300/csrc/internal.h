@@ -82,6 +82,24 @@ struct BlockCopyArgs {
 };
 int launch_block_copy(const BlockCopyArgs &a, cudaStream_t stream);
 
+// Multi-token append attention (pf_paged_prefill_attention).
+struct PrefillArgs {
+    const pf_pool *pool;
+    int layer;
+    const void *q;
+    const int32_t *block_tables;
+    int max_blocks;
+    const int32_t *context_lens;
+    const int32_t *cu_q;
+    int n_seqs;
+    int max_new;
+    int n_q_heads;
+    float scale;
+    void *out;
+    int out_dtype;
+};
+int launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+
 struct GatherArgs {
     const pf_pool *pool;
     int layer;

@@ -1,0 +1,89 @@
+"""pf_paged_prefill_attention (multi-token append: each sequence's last n_s
+tokens attend causally over its context) against the oracle, on mixed
+lengths, grouped heads, block sizes 1..256 and head_dim 64/128, including
+whole prompts and the write-then-attend flow."""
+import numpy as np
+import pytest
+
+import synth_inputs as si
+from gpu_util import MAX_ABS, MEAN_ABS, PagedCase, assert_close_to_oracle, dev, host
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(pkv, cuda_dev, c, n_new, scale, out_f32=False, seed=500):
+    import torch
+    cu = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    q = si.fp16_normal((int(cu[-1]), c.Hq, c.D), seed)
+    out = torch.full((int(cu[-1]), c.Hq, c.D), float("nan"),
+                     dtype=torch.float32 if out_f32 else torch.float16, device=cuda_dev)
+    pkv.pf_paged_prefill_attention(c.pool, 0, dev(q, cuda_dev), c.bt_dev, c.lens_dev, dev(cu, cuda_dev),
+                                   int(max(n_new.max(), 1)), scale, out)
+    torch.cuda.synchronize()
+    return q, cu, host(out)
+
+
+@pytest.mark.parametrize("hq,hkv,d,b", [(12, 12, 64, 16), (14, 2, 64, 1), (14, 2, 64, 256), (8, 4, 128, 64),
+                                        (40, 40, 128, 16), (16, 2, 64, 16)])
+def test_chunked_append_mixed_lengths(pkv, cuda_dev, oracle_mod, hq, hkv, d, b):
+    lens = si.uniform_lengths(24, 1, 700, seed=21)
+    rng = np.random.default_rng(5)
+    n_new = np.minimum(lens, rng.integers(0, 40, size=lens.size)).astype(np.int32)   # some 0, some all of L
+    n_new[3] = lens[3]
+    c = PagedCase(pkv, cuda_dev, lens, hq, hkv, d, b)
+    q, cu, got = _run(pkv, cuda_dev, c, n_new, 1.0 / np.sqrt(d))
+    ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, np.float32(1.0 / np.sqrt(d)))
+    assert_close_to_oracle(got, ref, what=f"prefill {hq}/{hkv}x{d} B={b}")
+    assert pkv.pf_device_status(reset=True) == 0
+
+
+def test_whole_prompts_fp32(pkv, cuda_dev, oracle_mod):
+    lens = np.array([1, 2, 15, 16, 17, 33, 100, 64], dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 6, 3, 64, 16)
+    q, cu, got = _run(pkv, cuda_dev, c, lens.copy(), 0.125, out_f32=True)
+    ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, 0.125)
+    assert_close_to_oracle(got, ref, max_abs=1e-5, mean_abs=1e-6, what="whole prompts")
+    # the first token of a prompt sees only itself: its output is V0
+    v0 = c.v_host[0, c.bt[0, 0], 0].astype(np.float32)          # sequence 0, token 0, all kv-heads
+    assert np.array_equal(got[0].reshape(3, 2, 64), np.repeat(v0[:, None, :], 2, axis=1))
+
+
+def test_write_prompt_then_attend(pkv, cuda_dev, oracle_mod):
+    """The prompt's K/V rows go into the pages with pf_write_kv, then its
+    queries attend: the pool and the outputs match the oracle doing the same."""
+    import torch
+    lens = si.uniform_lengths(10, 1, 200, seed=23)
+    c = PagedCase(pkv, cuda_dev, lens, 12, 12, 64, 16)
+    seq_idx = np.repeat(np.arange(lens.size), lens).astype(np.int32)
+    pos = np.concatenate([np.arange(L) for L in lens]).astype(np.int32)
+    kn = si.fp16_normal((seq_idx.size, 12, 64), 60)
+    vn = si.fp16_normal((seq_idx.size, 12, 64), 61)
+    pkv.pf_write_kv(c.pool, 0, dev(kn, cuda_dev), dev(vn, cuda_dev), c.bt_dev, dev(seq_idx, cuda_dev),
+                    dev(pos, cuda_dev))
+    oracle_mod.scatter(c.k_host, c.v_host, 0, kn, vn, c.bt, seq_idx, pos)
+    q, cu, got = _run(pkv, cuda_dev, c, lens.copy(), 0.125)
+    ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, 0.125)
+    assert_close_to_oracle(got, ref, what="write then attend")
+    assert np.array_equal(host(c.k_dev).view(np.uint16), c.k_host.view(np.uint16))
+
+
+def test_one_new_token_is_decode_attention(pkv, cuda_dev, oracle_mod):
+    lens = si.uniform_lengths(40, 1, 1500, seed=24)
+    c = PagedCase(pkv, cuda_dev, lens, 12, 12, 64, 16)
+    n_new = np.ones(lens.size, dtype=np.int32)
+    q, cu, got = _run(pkv, cuda_dev, c, n_new, 0.125)
+    assert_close_to_oracle(got, c.oracle(oracle_mod, 0.125, q=q), what="n_s = 1")
+
+
+def test_too_many_new_tokens_is_flagged(pkv, cuda_dev):
+    import torch
+    lens = np.array([5, 20], dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 4, 4, 64, 16)
+    cu = np.array([0, 9, 11], dtype=np.int32)                # 9 new tokens in a 5-token sequence
+    q = dev(si.fp16_normal((11, 4, 64), 70), cuda_dev)
+    out = torch.zeros((11, 4, 64), dtype=torch.float16, device=cuda_dev)
+    pkv.pf_device_status(reset=True)
+    pkv.pf_paged_prefill_attention(c.pool, 0, q, c.bt_dev, c.lens_dev, dev(cu, cuda_dev), 9, 0.125, out)
+    torch.cuda.synchronize()
+    assert pkv.pf_device_status(reset=True) & pkv.PF_DEV_BAD_LENGTH
+    assert np.all(np.isfinite(host(out)))
