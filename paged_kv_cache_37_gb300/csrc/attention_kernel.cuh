@@ -79,8 +79,8 @@ struct ItemDesc {
     int tok0;   // first token
     int ntok;   // tokens (>= 1)
     int kind;   // ItemKind
-    int a;      // kChunk: global chunk index; kSpanPart: flattened first tile of the pair
-    int b;      // kChunk: chunk index in the sequence; kSpanPart: tiles of the pair
+    int a;      // kChunk: global chunk index; kSpanPart: flattened first unit of the pair
+    int b;      // kChunk: chunk index in the sequence; kSpanPart: units of the pair
     int c;      // kChunk: chunks of the sequence; kSpanPart: record slot (0/1) in the span
     int span;   // kSpanPart: span index
     int newrow;   // fused step: token L - 1 when this item holds it, else -1
@@ -103,7 +103,15 @@ struct PendPart {
     int s, h0, first, z_first, n_parts;
 };
 
-constexpr int kMaxSeqsPerLaunch = 1024;   // the span schedule keeps lengths in shared memory
+constexpr int kMaxSeqsPerLaunch = 1024;
+
+// Span schedule: a (sequence, head-group) pair costs its tiles plus
+// kPairCost "cost units" in the partition.  Measured on the mixed workload,
+// a CTA spends about one tile's time more for each extra pair in its span
+// (CTAs with 4 pairs took ~3.5 us longer than CTAs with 1 for the same tile
+// count), so spans of many short pairs get fewer tiles.  The cost unit sits
+// at the pair's start and carries no work.
+constexpr int kPairCost = 1;   // the span schedule keeps lengths in shared memory
 
 struct Params {
     const __half *q;
@@ -179,9 +187,10 @@ struct __align__(128) Smem {
     uint64_t cbar;   // consumer-warps barrier (count NCW), used when WPH > 1
     PendPart pend[NCW][2];   // span schedule: this warp's cut parts (record slot 0 / 1)
     int warp_tot[NTHREADS / 32];
-    // span schedule: pre[s] = tiles (per group) of sequences before s, for
+    // span schedule: pre[s] = units (per group: tiles + kPairCost, 0 for an
+    // empty sequence) of sequences before s, for
     // s = 0..S; rem[s] = tokens of sequence s in its last tile (1..16), so
-    // its clamped length is (pre[s + 1] - pre[s] - 1) * 16 + rem[s]
+    // its clamped length is (pre[s + 1] - pre[s] - kPairCost - 1) * 16 + rem[s]
     int pre[kMaxSeqsPerLaunch + 1];
     uint8_t rem[kMaxSeqsPerLaunch];
 };
@@ -319,36 +328,44 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     } else {
         load_window(0);
     }
+    const long long sstart = x;
     auto decode_span = [&]() {
         ProdItem it;
-        it.done = x >= xend;
-        if (it.done) return it;
-        // largest s with pre[s] * ng <= x (it has tiles: pre[s + 1] * ng > x)
-        int lo = 0, hi = S - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if ((long long)sm.pre[mid] * ng <= x) lo = mid;
-            else hi = mid - 1;
+        for (;;) {
+            it.done = x >= xend;
+            if (it.done) return it;
+            // largest s with pre[s] * ng <= x (it has units: pre[s + 1] * ng > x)
+            int lo = 0, hi = S - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if ((long long)sm.pre[mid] * ng <= x) lo = mid;
+                else hi = mid - 1;
+            }
+            const int s = lo;
+            const int u = sm.pre[s + 1] - sm.pre[s];          // units of each of its pairs
+            const int nt = u - kPairCost;                     // tiles of each of its pairs
+            const long long pair0 = (long long)sm.pre[s] * ng;
+            const int grp = (int)((x - pair0) / u);
+            const long long a = pair0 + (long long)grp * u;    // the pair's first unit (its cost unit)
+            const int off = (int)(x - a);
+            const int len = (int)min((long long)(u - off), xend - x);
+            const int t0 = max(off - kPairCost, 0);           // the pair's tiles in this span
+            const int t1 = min(off + len - kPairCost, nt);
+            const bool first_segment = x == sstart;
+            x += len;
+            if (t1 <= t0) continue;                           // only the pair's cost unit: no work
+            it.s = s;
+            it.h0 = grp * HG;
+            it.tok0 = t0 * TB;
+            it.ntok = (t1 - t0) * TB;
+            it.kind = (t0 == 0 && t1 == nt) ? kWhole : kSpanPart;
+            it.a = (int)a;
+            it.b = u;
+            it.c = first_segment ? 0 : 1;
+            it.span = (int)span;
+            finish_decode(it, (nt - 1) * TB + sm.rem[s]);
+            return it;
         }
-        const int s = lo;
-        const int nt = sm.pre[s + 1] - sm.pre[s];
-        const long long pair0 = (long long)sm.pre[s] * ng;
-        const int grp = (int)((x - pair0) / nt);
-        const int t0 = (int)(x - pair0 - (long long)grp * nt);
-        const int len = (int)min((long long)(nt - t0), xend - x);
-        it.s = s;
-        it.h0 = grp * HG;
-        it.tok0 = t0 * TB;
-        it.ntok = len * TB;
-        const bool whole = t0 == 0 && len == nt;
-        it.kind = whole ? kWhole : kSpanPart;
-        it.a = (int)(pair0 + (long long)grp * nt);       // flattened first tile of the pair
-        it.b = nt;
-        it.c = (x == map.start(span)) ? 0 : 1;
-        it.span = (int)span;
-        x += len;
-        finish_decode(it, (nt - 1) * TB + sm.rem[s]);
-        return it;
     };
     auto decode = [&](int k) { return p.spans ? decode_span() : decode_chunk(k); };
 
@@ -909,13 +926,14 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 // slot 1 when the pair starts inside it.
                 write_part<D, G, HG>(p, sm, d, hl, lane, false, m, l, acc);
                 if (lane == 0) {
+                    // units a .. a + b - 1: the cost unit, then the tiles
                     const SpanMap map((long long)sm.pre[p.n_seqs] * p.n_groups, gridDim.x);
-                    const long long first = map.owner(d.a);
+                    const long long first = map.owner((long long)d.a + kPairCost);
                     PendPart pp;
                     pp.s = d.s;
                     pp.h0 = d.h0;
                     pp.first = (int)first;
-                    pp.z_first = d.a == map.start(first) ? 0 : 1;
+                    pp.z_first = (long long)d.a <= map.start(first) ? 0 : 1;   // the span's first segment?
                     pp.n_parts = (int)(map.owner((long long)d.a + d.b - 1) - first + 1);
                     sm.pend[cw][d.c] = pp;
                 }
@@ -969,7 +987,7 @@ __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const C
                 L = L < 0 ? 0 : maxctx;
             }
             sm.rem[s] = (uint8_t)(L - (L - 1) / TB * TB);   // unused when L = 0
-            sm.pre[s + 1] = (L + TB - 1) / TB;
+            sm.pre[s + 1] = L > 0 ? (L + TB - 1) / TB + kPairCost : 0;
         }
         __syncthreads();
         const int per = (S + NTHREADS - 1) / NTHREADS;
