@@ -374,6 +374,22 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     int posted = 0;    // item slots posted (including the final sentinel)
     bool ok = true;
     ProdItem it = decode(0);
+    // Pull the first ring's worth of tiles into L2 before waiting for the
+    // previous kernel.  A prefetch brings nothing into this CTA: the copies
+    // after the wait read the lines as they are then, with whatever the
+    // previous kernel wrote, but from L2 instead of DRAM.
+    if (!it.done && B >= TB) {
+        const int j = lane;                                // this lane's tile of item 0
+        const int tiles0 = (it.ntok + TB - 1) / TB;
+        const int t = it.tok0 + j * TB;
+        const int pa = j < tiles0 ? t / B - it.pg0 : 0;    // < NS <= 16: inside the id window
+        const int id = __shfl_sync(FULL, it.ids0, pa);
+        if (j < NS && j < tiles0 && id >= 0 && id < p.n_blocks) {
+            const int r = p.layer_row0 + id * B + (t % B);
+            tma_prefetch_3d(tmk, 0, it.h0, r);
+            tma_prefetch_3d(tmv, 0, it.h0, r);
+        }
+    }
     // Launched as a programmatic dependent: wait for the previous kernel on
     // the stream before the first read of q or the pool (a no-op otherwise).
     asm volatile("griddepcontrol.wait;" ::: "memory");

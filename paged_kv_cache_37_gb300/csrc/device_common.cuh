@@ -141,6 +141,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         : "memory");
 }
 
+// L2 prefetch of one tile through a tensor map: nothing is copied into the
+// CTA and no barrier is involved.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 // Order this thread's earlier generic-proxy global writes before its later
 // async-proxy (TMA) accesses of global memory.
 __device__ __forceinline__ void fence_proxy_async_global() {
