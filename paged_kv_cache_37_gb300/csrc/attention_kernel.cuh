@@ -143,6 +143,7 @@ struct Params {
 
     int out_f32;
     float scale_log2; // scale * log2(e)
+    int prefetch_tiles;   // tiles of the first item pulled into L2 before the dependency wait (<= 32)
 };
 
 // Span map of the span schedule: the W flattened tiles cut into
@@ -374,17 +375,18 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     int posted = 0;    // item slots posted (including the final sentinel)
     bool ok = true;
     ProdItem it = decode(0);
-    // Pull the first ring's worth of tiles into L2 before waiting for the
-    // previous kernel.  A prefetch brings nothing into this CTA: the copies
-    // after the wait read the lines as they are then, with whatever the
-    // previous kernel wrote, but from L2 instead of DRAM.
+    // Pull the first tiles into L2 before waiting for the previous kernel
+    // (prefetch_tiles of them: deeper when this launch overlaps one).  A
+    // prefetch brings nothing into this CTA: the copies after the wait read
+    // the lines as they are then, with whatever the previous kernel wrote,
+    // but from L2 instead of DRAM.
     if (!it.done && B >= TB) {
         const int j = lane;                                // this lane's tile of item 0
         const int tiles0 = (it.ntok + TB - 1) / TB;
         const int t = it.tok0 + j * TB;
-        const int pa = j < tiles0 ? t / B - it.pg0 : 0;    // < NS <= 16: inside the id window
+        const int pa = j < tiles0 ? t / B - it.pg0 : 0;    // <= j < 32: inside the id window
         const int id = __shfl_sync(FULL, it.ids0, pa);
-        if (j < NS && j < tiles0 && id >= 0 && id < p.n_blocks) {
+        if (j < p.prefetch_tiles && j < tiles0 && id >= 0 && id < p.n_blocks) {
             const int r = p.layer_row0 + id * B + (t % B);
             tma_prefetch_3d(tmk, 0, it.h0, r);
             tma_prefetch_3d(tmv, 0, it.h0, r);
