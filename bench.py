@@ -302,17 +302,19 @@ def run_ours(args, dist):
     sp = ctypes.c_void_p(stream.cuda_stream)
     P = lambda t: ctypes.c_void_p(t.data_ptr())
 
-    def arg_sets(layout):
+    def arg_sets(layout, overlap=True):
         bt = tables[layout]
         ws_ = [(P(r["ws"]), r["ws"].numel()) for r in reps]
         wr = [(r["pool"].handle, 0, P(r["kn"]), P(r["vn"]), P(bt), S, maxb, P(seq_d), P(pos_d), S, sp) for r in reps]
         at = [(r["pool"].handle, 0, P(r["q"]), P(bt), maxb, P(lens_d), S, Hq, ctypes.c_float(w["scale"]),
                P(r["out"]), pkv.PF_F16, args.split, ws_[i][0], ws_[i][1], sp) for i, r in enumerate(reps)]
         # consecutive steps write neither the lengths nor the tables, so each
-        # step's launch may overlap the previous step's kernel
+        # step's launch may overlap the previous step's kernel; a call timed
+        # on its own (events around it) has nothing to overlap and does not ask
+        flag = 0 if overlap is False else pkv.PF_STEP_OVERLAP_PREVIOUS
         fu = [(r["pool"].handle, 0, P(r["q"]), P(r["kn"]), P(r["vn"]), P(bt), maxb, P(lens_d), S, Hq,
                ctypes.c_float(w["scale"]), P(r["out"]), pkv.PF_F16, args.split, ws_[i][0], ws_[i][1],
-               pkv.PF_STEP_OVERLAP_PREVIOUS, sp)
+               flag, sp)
               for i, r in enumerate(reps)]
         return wr, at, fu
 
@@ -321,7 +323,7 @@ def run_ours(args, dist):
             raise pkv.PagedKVError(rc, pkv.pf_last_error())
 
     def run_steps(layout, n, events=None, fused=True):
-        wr, at, fu = arg_sets(layout)
+        wr, at, fu = arg_sets(layout, overlap=events is None)
         for i in range(n):
             r = i % R
             if events is not None:
