@@ -79,7 +79,7 @@ typedef struct pf_alloc pf_alloc;
 PF_API const char *pf_last_error(void);
 
 /* ABI version of this header (PF_ABI_VERSION). */
-#define PF_ABI_VERSION 2
+#define PF_ABI_VERSION 3
 PF_API int pf_abi_version(void);
 
 /* ------------------------------------------------------------- pool ---- */
@@ -298,7 +298,15 @@ PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
  * [n_seqs + 1], non-decreasing; max_new_tokens bounds every n_s (it sizes
  * the grid).  On the device, n_s > L or > max_new_tokens, or a length
  * outside the table, sets PF_DEV_BAD_LENGTH and is clamped; bad block ids set
- * PF_DEV_BAD_BLOCK_ID.  No workspace. */
+ * PF_DEV_BAD_BLOCK_ID.
+ * Two kernels: with a workspace (of pf_prefill_workspace_bytes bytes,
+ * initialised once with pf_decode_workspace_init, not shared by overlapping
+ * calls) and max_new_tokens x (n_q_heads / Hkv) <= 8, the decode kernel
+ * serves the new tokens as extra rows of each kv-head -- balanced spans over
+ * the contexts, every K/V byte read once per kv-head (a chunked append);
+ * otherwise (workspace null, or longer appends and prompts) a kernel that
+ * needs no workspace walks each (chunk of new tokens, kv-head) over its
+ * context. */
 PF_API int pf_paged_prefill_attention(const pf_pool *pool, int layer,
                                       const void *q,
                                       const int32_t *block_tables,
@@ -307,7 +315,14 @@ PF_API int pf_paged_prefill_attention(const pf_pool *pool, int layer,
                                       const int32_t *cu_q, int n_seqs,
                                       int max_new_tokens, int n_q_heads,
                                       float scale, void *out, int out_dtype,
+                                      void *workspace, size_t ws_bytes,
                                       void *stream);
+/* Workspace bytes of pf_paged_prefill_attention's decode-kernel path for
+ * these sizes, or 0 when that path does not apply (more than 8 rows per
+ * kv-head; the call then needs no workspace) or on bad arguments. */
+PF_API size_t pf_prefill_workspace_bytes(const pf_pool *pool, int n_seqs,
+                                         int n_q_heads, int max_blocks_per_seq,
+                                         int max_new_tokens);
 
 /* The decode attention call for callers that cannot allocate device memory.
  * No counterpart on the pages: it exists for code that may only touch the

@@ -19,10 +19,22 @@ from ._native import (  # noqa: F401
     pf_swap_out,
     pf_decode_step, pf_decode_workspace_bytes, pf_decode_workspace_init, pf_device_status, pf_free_blocks,
     pf_gather_kv, pf_last_error, pf_paged_decode_attention, pf_paged_decode_attention_noalloc,
-    pf_paged_prefill_attention,
+    pf_paged_prefill_attention, pf_prefill_workspace_bytes,
     pf_pool_bytes, pf_pool_create,
     pf_pool_destroy, pf_seq_release, pf_seq_reserve, pf_write_kv,
 )
+
+
+def make_prefill_workspace(pool, n_seqs, n_q_heads, max_blocks_per_seq, max_new_tokens, device=None):
+    """Allocate (with torch) and initialise a workspace for the decode-kernel
+    path of pf_paged_prefill_attention; None when that path does not apply."""
+    import torch
+    nbytes = pf_prefill_workspace_bytes(pool, n_seqs, n_q_heads, max_blocks_per_seq, max_new_tokens)
+    if nbytes == 0:
+        return None
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=device or pool.k_pool.device)
+    pf_decode_workspace_init(ws)
+    return ws
 
 
 def make_workspace(pool, n_seqs, n_q_heads, max_blocks_per_seq, split_tokens=0, device=None):

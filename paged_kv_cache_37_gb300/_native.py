@@ -80,7 +80,8 @@ def lib():
         "pf_alloc_cow": (I, [P, P, P, P]),
         "pf_seq_fork": (I, [P, I, P, I, P, I]),
         "pf_block_image_bytes": (Z, [P]),
-        "pf_paged_prefill_attention": (I, [P, I, P, P, I, P, P, I, I, I, F, P, I, P]),
+        "pf_paged_prefill_attention": (I, [P, I, P, P, I, P, P, I, I, I, F, P, I, P, Z, P]),
+        "pf_prefill_workspace_bytes": (Z, [P, I, I, I, I]),
         "pf_copy_blocks": (I, [P, P, P, I, P]),
         "pf_swap_out": (I, [P, P, I, P, P]),
         "pf_swap_in": (I, [P, P, P, I, P]),
@@ -309,10 +310,17 @@ def pf_swap_in(pool, host_src, ids, stream=None):
     _check(lib().pf_swap_in(pool.handle, ptr, _dev_ptr(ids, "ids", torch.int32), n, _stream_ptr(stream)))
 
 
+def pf_prefill_workspace_bytes(pool, n_seqs, n_q_heads, max_blocks_per_seq, max_new_tokens):
+    """Workspace bytes of the decode-kernel path of pf_paged_prefill_attention
+    (0: that path does not apply, no workspace needed)."""
+    return lib().pf_prefill_workspace_bytes(pool.handle, n_seqs, n_q_heads, max_blocks_per_seq, max_new_tokens)
+
+
 def pf_paged_prefill_attention(pool, layer, q, block_tables, context_lens, cu_q, max_new_tokens, scale, out,
-                               stream=None):
+                               workspace=None, stream=None):
     """Causal attention of each sequence's last n_s = cu_q[s+1] - cu_q[s]
-    tokens (q rows cu_q[s]..cu_q[s+1]-1) over its context (device tensors)."""
+    tokens (q rows cu_q[s]..cu_q[s+1]-1) over its context (device tensors).
+    With a workspace, short appends run on the decode kernel."""
     import torch
     n = context_lens.numel()
     if block_tables.dim() != 2 or block_tables.shape[0] != n or cu_q.numel() != n + 1:
@@ -326,7 +334,9 @@ def pf_paged_prefill_attention(pool, layer, q, block_tables, context_lens, cu_q,
         pool.handle, layer, _dev_ptr(q, "q", torch.float16), _dev_ptr(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32),
         _dev_ptr(cu_q, "cu_q", torch.int32), n, int(max_new_tokens), q.shape[1], float(scale),
-        _dev_ptr(out, "out"), out_dtype, _stream_ptr(stream)))
+        _dev_ptr(out, "out"), out_dtype,
+        None if workspace is None else _dev_ptr(workspace, "workspace"),
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _stream_ptr(stream)))
 
 
 def pf_write_kv(pool, layer, k_new, v_new, block_tables, seq_idx, pos, stream=None):

@@ -266,8 +266,8 @@ static int decode_call(const pf_pool *pool, int layer, const void *q, const void
                                                   std::to_string(ws_bytes) + " bytes, needs " +
                                                   std::to_string(need));
     pkv::AttnArgs a{const_cast<pf_pool *>(pool), layer, q, k_new, v_new, overlap_previous, block_tables,
-                    max_blocks_per_seq, context_lens, n_seqs, n_q_heads, scale, out, out_dtype, plan, workspace,
-                    ws_bytes};
+                    max_blocks_per_seq, context_lens, n_seqs, n_q_heads, n_q_heads / pool->n_kv_heads, nullptr,
+                    scale, out, out_dtype, plan, workspace, ws_bytes};
     return pkv::launch_attention(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -298,10 +298,33 @@ int pf_decode_step(const pf_pool *pool, int layer, const void *q, const void *k_
                        n_q_heads, scale, out, out_dtype, split_tokens, workspace, ws_bytes, stream);
 }
 
+// Rows per kv-head when an append takes the decode kernel (its query tokens
+// x its q-heads), or 0 when they do not fit (the standalone kernel then).
+static int append_rows(const pf_pool *pool, int n_q_heads, int max_new_tokens) {
+    if (n_q_heads <= 0 || n_q_heads % pool->n_kv_heads) return 0;
+    const long long rows = (long long)max_new_tokens * (n_q_heads / pool->n_kv_heads);
+    return rows >= 1 && rows <= 8 ? (int)rows : 0;
+}
+
+size_t pf_prefill_workspace_bytes(const pf_pool *pool, int n_seqs, int n_q_heads, int max_blocks_per_seq,
+                                  int max_new_tokens) {
+    pkv::clear_error();
+    if (!pool || n_seqs < 0 || max_blocks_per_seq <= 0 || max_new_tokens < 0) {
+        pkv::set_error(PF_ERR_INVALID, "pf_prefill_workspace_bytes: bad arguments");
+        return 0;
+    }
+    const int rows = append_rows(pool, n_q_heads, max_new_tokens);
+    if (rows == 0) return 0;   // the call takes the kernel that needs no workspace
+    pkv::AttnPlan plan;
+    if (pkv::attention_plan(pool, n_seqs, rows * pool->n_kv_heads, max_blocks_per_seq, 0, true, &plan) != PF_OK)
+        return 0;
+    return plan.counter_bytes + plan.partial_bytes;
+}
+
 int pf_paged_prefill_attention(const pf_pool *pool, int layer, const void *q, const int32_t *block_tables,
                                int max_blocks_per_seq, const int32_t *context_lens, const int32_t *cu_q, int n_seqs,
                                int max_new_tokens, int n_q_heads, float scale, void *out, int out_dtype,
-                               void *stream) {
+                               void *workspace, size_t ws_bytes, void *stream) {
     pkv::clear_error();
     int rc = check_pool(pool, layer, "pf_paged_prefill_attention");
     if (rc) return rc;
@@ -323,6 +346,25 @@ int pf_paged_prefill_attention(const pf_pool *pool, int layer, const void *q, co
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: bad max_blocks_per_seq");
     if (!(scale > 0.0f) || scale != scale)
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: scale must be a positive number");
+    const int rows = append_rows(pool, n_q_heads, max_new_tokens);
+    if (workspace != nullptr && rows > 0) {
+        // The decode kernel, its G rows per kv-head being the query tokens x
+        // q-heads: balanced spans over the contexts, merged in the kernel.
+        if (!aligned16(workspace))
+            return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: workspace must be 16-byte aligned");
+        pkv::AttnPlan plan;
+        rc = pkv::attention_plan(pool, n_seqs, rows * pool->n_kv_heads, max_blocks_per_seq, 0, true, &plan);
+        if (rc) return rc;
+        const size_t need = plan.counter_bytes + plan.partial_bytes;
+        if (ws_bytes < need)
+            return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: workspace has " +
+                                                      std::to_string(ws_bytes) + " bytes, needs " +
+                                                      std::to_string(need));
+        pkv::AttnArgs a{const_cast<pf_pool *>(pool), layer, q, nullptr, nullptr, false, block_tables,
+                        max_blocks_per_seq, context_lens, n_seqs, n_q_heads, rows, cu_q, scale, out, out_dtype, plan,
+                        workspace, ws_bytes};
+        return pkv::launch_attention(a, static_cast<cudaStream_t>(stream));
+    }
     pkv::PrefillArgs a{pool, layer, q, block_tables, max_blocks_per_seq, context_lens, cu_q, n_seqs, max_new_tokens,
                        n_q_heads, scale, out, out_dtype};
     return pkv::launch_prefill(a, static_cast<cudaStream_t>(stream));

@@ -199,7 +199,7 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     if (!status) return PF_ERR_CUDA;
     KernelInfo ki;
     int HG = 0;
-    rc = kernel_for(pool, a.n_q_heads, &ki, &HG);
+    rc = kernel_for(pool, a.rows * pool->n_kv_heads, &ki, &HG);
     if (rc) return rc;
     const AttnPlan &plan = a.plan;
 
@@ -230,6 +230,7 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     // CTAs, 16 tiles is about the size of L2); called alone, 16 tiles cost
     // 2 us more than 4.
     p.prefetch_tiles = a.overlap_previous ? 16 : 4;
+    p.gh = a.n_q_heads / pool->n_kv_heads;
     const size_t out_elem = a.out_dtype == PF_F32 ? 4 : 2;
     const size_t row = (size_t)a.n_q_heads * pool->head_dim;   // q / out elements per sequence
 
@@ -238,11 +239,15 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     // stamps its merge jobs with a fresh epoch.
     for (int s0 = 0; s0 < a.n_seqs; s0 += attn::kMaxSeqsPerLaunch) {
         const int n = a.n_seqs - s0 < attn::kMaxSeqsPerLaunch ? a.n_seqs - s0 : attn::kMaxSeqsPerLaunch;
-        p.q = static_cast<const __half *>(a.q) + (size_t)s0 * row;
+        // decode: q and out rows are the sequences; append: cu_q holds
+        // absolute rows, so only it moves with the launch
+        const size_t qoff = a.cu_q ? 0 : (size_t)s0 * row;
+        p.cu_q = a.cu_q ? a.cu_q + s0 : nullptr;
+        p.q = static_cast<const __half *>(a.q) + qoff;
         const size_t kv_row = (size_t)pool->n_kv_heads * pool->head_dim;
         p.k_new = a.k_new ? static_cast<const __half *>(a.k_new) + (size_t)s0 * kv_row : nullptr;
         p.v_new = a.v_new ? static_cast<const __half *>(a.v_new) + (size_t)s0 * kv_row : nullptr;
-        p.out = static_cast<uint8_t *>(a.out) + (size_t)s0 * row * out_elem;
+        p.out = static_cast<uint8_t *>(a.out) + qoff * out_elem;
         p.bt = a.block_tables + (size_t)s0 * a.max_blocks;
         p.lens = a.context_lens + s0;
         p.n_seqs = n;

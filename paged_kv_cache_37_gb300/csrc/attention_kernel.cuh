@@ -85,6 +85,9 @@ struct ItemDesc {
     int span;   // kSpanPart: span index
     int newrow;   // fused step: token L - 1 when this item holds it, else -1
     int newslot;  // fused step: pool row of token L - 1 (-1: bad block id, not written)
+    int L;        // the sequence's (clamped) length
+    int nq;       // its query tokens (1 for decode; the new tokens of an append)
+    int qrow0;    // q / out row of its first query token
     int pad0;
 };
 
@@ -100,7 +103,7 @@ struct Job {
 // A part of a cut pair that a consumer warp finished (span schedule): the
 // pair's output location and the span records that hold its parts.
 struct PendPart {
-    int s, h0, first, z_first, n_parts;
+    int s, h0, first, z_first, n_parts, qrow0, nq;
 };
 
 constexpr int kMaxSeqsPerLaunch = 1024;
@@ -144,6 +147,12 @@ struct Params {
     int out_f32;
     float scale_log2; // scale * log2(e)
     int prefetch_tiles;   // tiles of the first item pulled into L2 before the dependency wait (<= 32)
+    // Append (multi-token) attention: sequence s's query tokens are q rows
+    // cu_q[s] .. cu_q[s + 1] - 1, the last positions of its L tokens, each
+    // attending causally.  Null for decode (one query per sequence, row s).
+    // A kv-head's G rows are its query tokens x its gh q-heads.
+    const int32_t *cu_q;
+    int gh;               // q-heads per kv-head (G for decode)
 };
 
 // Span map of the span schedule: the W flattened tiles cut into
@@ -217,6 +226,16 @@ __device__ __forceinline__ void prefetch_table_rows(const Params &p) {
     }
 }
 
+// Append: a sequence without query tokens has no work (length 0); more
+// query tokens than its length or than the G rows hold is flagged (and
+// clamped where the tokens are read).  Decode: the length as is.
+__device__ __forceinline__ int append_length(const Params &p, int s, int L, int G) {
+    if (p.cu_q == nullptr) return L;
+    const int nq = p.cu_q[s + 1] - p.cu_q[s];
+    if (nq < 0 || nq > L || nq * p.gh > G) atomicOr(p.status, PF_DEV_BAD_LENGTH);
+    return nq > 0 ? L : 0;
+}
+
 // ------------------------------------------------------------ producer
 
 struct ProdItem {
@@ -224,6 +243,7 @@ struct ProdItem {
     int s, h0, tok0, ntok, kind, a, b, c, span, pg0, npg, L;
     int last_id;      // fused step: raw block id of token L - 1 when the item holds it
     int ids0, ids1;   // raw block ids of pages pg0 + lane and pg0 + 32 + lane
+    int qrow0, nq;    // q row of the sequence's first query token; its query tokens
 };
 
 template <int D, int G, int HG>
@@ -259,6 +279,15 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         // its newest token; its page's block id is needed when it is posted.
         it.last_id = (p.k_new != nullptr && it.tok0 + it.ntok == L)
                          ? p.bt[(size_t)it.s * p.max_blocks + (L - 1) / B] : 0;
+        // Append: the sequence's query tokens (clamped as the length scan
+        // flagged them); decode: one, at row s.
+        if (p.cu_q != nullptr) {
+            it.qrow0 = p.cu_q[it.s];
+            it.nq = max(1, min(min(p.cu_q[it.s + 1] - it.qrow0, L), G / p.gh));
+        } else {
+            it.qrow0 = it.s;
+            it.nq = 1;
+        }
     };
 
     // ---- chunk schedule: 32-sequence window of the chunk numbering: per lane
@@ -274,6 +303,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
                 atomicOr(p.status, PF_DEV_BAD_LENGTH);
                 L = L < 0 ? 0 : maxctx;
             }
+            L = append_length(p, s, L, G);
         }
         wl = L;
         wu = (L + C - 1) / C;
@@ -429,20 +459,29 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
                 else
                     atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);   // attended to, not written
             }
+            d.L = it.L;
+            d.nq = it.nq;
+            d.qrow0 = it.qrow0;
             d.pad0 = 0;
             sm.desc[slot] = d;
+            // q: one bulk copy per query token, its nv heads x gh q-heads
+            // (contiguous in q) to rows (i * HG + hl) * gh + g of the slot
             const int nv = min(HG, p.n_kv_heads - it.h0);           // heads that exist
-            const uint32_t qbytes = (uint32_t)nv * G * D * 2;
+            const uint32_t tokbytes = (uint32_t)nv * p.gh * D * 2;
             const uint32_t rowbytes = (uint32_t)nv * D * 2;
             const uint32_t qfull = smem_addr(&sm.qfull[slot]);
-            mbar_arrive_expect_tx(qfull, qbytes + (writes_new ? 2 * rowbytes : 0));
-            bulk_load(smem_addr(sm.q[slot]), p.q + ((size_t)it.s * p.n_q_heads + (size_t)it.h0 * G) * D, qbytes,
-                      qfull);
+            mbar_arrive_expect_tx(qfull, (uint32_t)it.nq * tokbytes + (writes_new ? 2 * rowbytes : 0));
             if (writes_new) {
                 const size_t src = ((size_t)it.s * p.n_kv_heads + it.h0) * D;
                 bulk_load(smem_addr(sm.knew[slot][0]), p.k_new + src, rowbytes, qfull);
                 bulk_load(smem_addr(sm.knew[slot][1]), p.v_new + src, rowbytes, qfull);
             }
+        }
+        __syncwarp();   // the expected bytes are set before any copy can complete
+        if (lane < it.nq) {
+            bulk_load(smem_addr(sm.q[slot] + (size_t)lane * HG * p.gh * D),
+                      p.q + ((size_t)(it.qrow0 + lane) * p.n_q_heads + (size_t)it.h0 * p.gh) * D,
+                      (uint32_t)min(HG, p.n_kv_heads - it.h0) * p.gh * D * 2, smem_addr(&sm.qfull[slot]));
         }
         ++posted;
 
@@ -536,11 +575,13 @@ __device__ __forceinline__ void store_whole(const Params &p, const ItemDesc &d, 
     if (lane < LPT) {
 #pragma unroll
         for (int g = 0; g < G; ++g) {
+            const int i = g / p.gh;               // query token of row g
+            if (i >= d.nq) continue;
             float x[8];
             const float inv = 1.0f / l[g];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) x[i] = acc[g][i] * inv;
-            store8(p, ((size_t)d.s * p.n_q_heads + (size_t)h * G + g) * D + lane * 8, x);
+            for (int e = 0; e < 8; ++e) x[e] = acc[g][e] * inv;
+            store8(p, ((size_t)(d.qrow0 + i) * p.n_q_heads + (size_t)h * p.gh + g - i * p.gh) * D + lane * 8, x);
         }
     }
 }
@@ -590,8 +631,8 @@ __device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG>
 // loads one part's (m, l) and, in the same round trip, every part's acc
 // values of its own dims (D / 32 of them), PB parts at a time.
 template <int D, int G, int HG>
-__device__ __forceinline__ void merge_pair(const Params &p, int kind, int first, int z_first, int n, int s, int h,
-                                           int hl, int lane) {
+__device__ __forceinline__ void merge_pair(const Params &p, int kind, int first, int z_first, int n, int qrow0,
+                                           int nq, int h, int hl, int lane) {
     constexpr int REC = G * (D + 2);
     constexpr int DPL = D / 32;   // dims per lane
     constexpr int PB = 8;         // parts whose acc loads are in flight together
@@ -603,6 +644,8 @@ __device__ __forceinline__ void merge_pair(const Params &p, int kind, int first,
     };
 #pragma unroll 1
     for (int g = 0; g < G; ++g) {
+        const int qi = g / p.gh;                  // query token of row g
+        if (qi >= nq) break;
         float mx = -INFINITY, ls = 0.0f;
         float a[DPL];
 #pragma unroll
@@ -655,7 +698,7 @@ __device__ __forceinline__ void merge_pair(const Params &p, int kind, int first,
         const float inv = 1.0f / ls;
 #pragma unroll
         for (int q = 0; q < DPL; ++q) {
-            const size_t o = ((size_t)s * Hq + (size_t)h * G + g) * D + lane + 32 * q;
+            const size_t o = ((size_t)(qrow0 + qi) * Hq + (size_t)h * p.gh + g - qi * p.gh) * D + lane + 32 * q;
             if (p.out_f32) static_cast<float *>(p.out)[o] = a[q] * inv;
             else static_cast<__half *>(p.out)[o] = __float2half_rn(a[q] * inv);
         }
@@ -679,11 +722,14 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
 
     // (as in the producer: the previous kernel may still be writing `out`)
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    // Empty (or invalid, clamped to empty) sequences get a zero output.
+    // Empty (or invalid, clamped to empty) sequences get a zero output
+    // (decode: row s; append: its query rows, when it has any).
     for (int s = blockIdx.x; s < p.n_seqs; s += gridDim.x) {
         if (p.lens[s] <= 0) {
-            for (int e = cw * 32 + lane; e < Hq * D; e += NCW * 32) {
-                const size_t o = (size_t)s * Hq * D + e;
+            const int r0 = p.cu_q != nullptr ? p.cu_q[s] : s;
+            const int nr = p.cu_q != nullptr ? p.cu_q[s + 1] - r0 : 1;
+            for (long long e = cw * 32 + lane; e < (long long)nr * Hq * D; e += NCW * 32) {
+                const size_t o = (size_t)r0 * Hq * D + e;
                 if (p.out_f32) static_cast<float *>(p.out)[o] = 0.0f;
                 else static_cast<__half *>(p.out)[o] = __float2half_rn(0.0f);
             }
@@ -730,11 +776,11 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                     if (lane == 0) fence_acq_rel_gpu();
                     __syncwarp();
                     if (last0)
-                        merge_pair<D, G, HG>(p, kSpanPart, pp0.first, pp0.z_first, pp0.n_parts, pp0.s, pp0.h0 + hl,
-                                             hl, lane);
+                        merge_pair<D, G, HG>(p, kSpanPart, pp0.first, pp0.z_first, pp0.n_parts, pp0.qrow0, pp0.nq,
+                                             pp0.h0 + hl, hl, lane);
                     if (last1)
-                        merge_pair<D, G, HG>(p, kSpanPart, pp1.first, pp1.z_first, pp1.n_parts, pp1.s, pp1.h0 + hl,
-                                             hl, lane);
+                        merge_pair<D, G, HG>(p, kSpanPart, pp1.first, pp1.z_first, pp1.n_parts, pp1.qrow0, pp1.nq,
+                                             pp1.h0 + hl, hl, lane);
                 }
             }
             return;
@@ -742,15 +788,22 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
         const int h = d.h0 + hl;
         const bool active = h < p.n_kv_heads;   // ragged last group: idle warps keep the protocol
 
+        // Row g of the head: query token g / gh, q-head g % gh; it sees
+        // tokens 0 .. lim[g] (L - 1 for decode; causal for an append).
         float qf[G][8];
+        int lim[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-            if (active) {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(&sm.q[slot][(hl * G + g) * D + sub * 8]);
+            const int i = g / p.gh;
+            const bool valid = active && i < d.nq;
+            lim[g] = valid ? d.L - d.nq + i : -1;
+            if (valid) {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(
+                    &sm.q[slot][((i * HG + hl) * p.gh + g - i * p.gh) * D + sub * 8]);
                 half8_to_float(raw, qf[g]);
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) qf[g][i] = active ? qf[g][i] * p.scale_log2 : 0.0f;
+            for (int e = 0; e < 8; ++e) qf[g][e] = valid ? qf[g][e] * p.scale_log2 : 0.0f;
         }
         // Fused decode step: the new token's rows stand in for the tile's row
         // L - 1 (whatever the tile read there), and the first warp of each
@@ -779,7 +832,6 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
         }
 
         const int ntiles = (d.ntok + TB - 1) / TB;
-        const int tend = d.tok0 + d.ntok;
         for (int j = 0; j < ntiles; ++j, ++st) {
             const int stage = st % NS;
             if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane)) return;
@@ -787,7 +839,8 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 const __half *kt = sm.k[stage];
                 const __half *vt = sm.v[stage];
                 const int tile0 = d.tok0 + j * TB;
-                const bool ragged = tile0 + TB > tend;     // only the last tile of an item
+                // tiles that reach a row's limit or the sequence's end
+                const bool masked = tile0 + TB > d.L - d.nq;
                 const int newr = (d.newrow >= 0 && j == ntiles - 1) ? d.newrow - tile0 : -1;   // row of token L - 1
                 // phase 1: this lane group's scores for all of the warp's steps
                 // (independent chains: loads, dots and shuffles interleave)
@@ -819,13 +872,13 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                         for (int g = 0; g < G; ++g) z[step][g] += __shfl_xor_sync(FULL, z[step][g], o);
                     }
                 }
-                if (ragged) {
+                if (masked) {
 #pragma unroll
                     for (int step = 0; step < STEPS; ++step) {
-                        if (tile0 + part * TPT + step * TPW + grp >= tend) {
+                        const int tok = tile0 + part * TPT + step * TPW + grp;
 #pragma unroll
-                            for (int g = 0; g < G; ++g) z[step][g] = -INFINITY;
-                        }
+                        for (int g = 0; g < G; ++g)
+                            if (tok > lim[g]) z[step][g] = -INFINITY;
                     }
                 }
                 // phase 2: the warp's maximum over the tile; the reference
@@ -858,14 +911,14 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 for (int step = 0; step < STEPS; ++step) {
                     float vf[8];
                     half8_to_float(vraw[step], vf);
-                    if (ragged && tile0 + part * TPT + step * TPW + grp >= tend) {
+                    if (masked && tile0 + part * TPT + step * TPW + grp >= d.L) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) vf[i] = 0.0f;   // tail rows may hold anything
                     }
 #pragma unroll
                     for (int g = 0; g < G; ++g) {
                         // a masked score has weight 0 (also when m is still -inf)
-                        const float pz = (ragged && z[step][g] == -INFINITY) ? 0.0f : exp2f(z[step][g] - m[g]);
+                        const float pz = (masked && z[step][g] == -INFINITY) ? 0.0f : exp2f(z[step][g] - m[g]);
                         l[g] += pz;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) acc[g][i] = fmaf(pz, vf[i], acc[g][i]);
@@ -953,6 +1006,8 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                     pp.first = (int)first;
                     pp.z_first = (long long)d.a <= map.start(first) ? 0 : 1;   // the span's first segment?
                     pp.n_parts = (int)(map.owner((long long)d.a + d.b - 1) - first + 1);
+                    pp.qrow0 = d.qrow0;
+                    pp.nq = d.nq;
                     sm.pend[cw][d.c] = pp;
                 }
                 pending |= 1 << d.c;
@@ -1004,6 +1059,7 @@ __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const C
                 atomicOr(p.status, PF_DEV_BAD_LENGTH);
                 L = L < 0 ? 0 : maxctx;
             }
+            L = append_length(p, s, L, G);
             sm.rem[s] = (uint8_t)(L - (L - 1) / TB * TB);   // unused when L = 0
             sm.pre[s + 1] = L > 0 ? (L + TB - 1) / TB + kPairCost : 0;
         }
@@ -1072,7 +1128,12 @@ __global__ void __launch_bounds__(128, 1) merge_kernel(const Params p, int n_job
         const int hl = (int)(wi - (long long)j * HG);
         const Job jb = p.jobs[j];
         if (jb.epoch != p.epoch || jb.h0 + hl >= p.n_kv_heads) continue;
-        merge_pair<D, G, HG>(p, jb.kind, jb.first, jb.z_first, jb.n_parts, jb.s, jb.h0 + hl, hl, lane);
+        int qrow0 = jb.s, nq = 1;
+        if (p.cu_q != nullptr) {
+            qrow0 = p.cu_q[jb.s];
+            nq = max(1, min(p.cu_q[jb.s + 1] - qrow0, G / p.gh));
+        }
+        merge_pair<D, G, HG>(p, jb.kind, jb.first, jb.z_first, jb.n_parts, qrow0, nq, jb.h0 + hl, hl, lane);
     }
 }
 

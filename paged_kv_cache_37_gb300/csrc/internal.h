@@ -138,6 +138,10 @@ struct AttnArgs {
     const int32_t *context_lens;
     int n_seqs;
     int n_q_heads;
+    // rows per kv-head: its q-heads for decode; for an append (cu_q set),
+    // the most query tokens of a sequence x its q-heads (at most 8)
+    int rows;
+    const int32_t *cu_q;   // append: query rows of sequence s are cu_q[s] .. cu_q[s + 1] - 1
     float scale;
     void *out;
     int out_dtype;

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol(pkv):
 
 
 def test_abi_version(pkv):
-    assert pkv.pf_abi_version() == 2
+    assert pkv.pf_abi_version() == 3
 
 
 def test_pool_bytes(pkv):
@@ -112,13 +112,15 @@ def test_device_calls_reject_bad_arguments_before_launch(pkv):
     assert lib.pf_swap_in(pool, None, None, 0, None) == pkv.PF_OK
     # prefill: q-heads not a multiple, group > 8, unaligned q, negative counts; no new token is a no-op
     pre = lambda hq=12, qp=ok, n=4, mx=3, dt=1: (pool, 0, qp, ok, 7, ok, ok, n, mx, hq, ctypes.c_float(0.125), ok,
-                                                 dt, None)
+                                                 dt, None, 0, None)
     assert lib.pf_paged_prefill_attention(*pre(hq=13)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_prefill_attention(*pre(hq=12 * 9)) == pkv.PF_ERR_UNSUPPORTED
     assert lib.pf_paged_prefill_attention(*pre(qp=P(0x30004))) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_prefill_attention(*pre(n=-1)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_prefill_attention(*pre(dt=7)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_prefill_attention(*pre(mx=0)) == pkv.PF_OK
+    assert lib.pf_prefill_workspace_bytes(pool, 4, 12, 7, 9) == 0        # 9 rows per kv-head: no workspace path
+    assert lib.pf_prefill_workspace_bytes(pool, 4, 12, 0, 2) == 0        # bad table width
     lib.pf_pool_destroy(pool)
 
 

@@ -87,3 +87,56 @@ def test_too_many_new_tokens_is_flagged(pkv, cuda_dev):
     torch.cuda.synchronize()
     assert pkv.pf_device_status(reset=True) & pkv.PF_DEV_BAD_LENGTH
     assert np.all(np.isfinite(host(out)))
+
+
+def _run_ws(pkv, cuda_dev, c, n_new, scale, seed=500):
+    """The decode-kernel path: a workspace, at most 8 rows per kv-head."""
+    import torch
+    cu = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    mx = int(max(n_new.max(), 1))
+    ws = pkv.make_prefill_workspace(c.pool, len(n_new), c.Hq, c.bt.shape[1], mx)
+    assert ws is not None
+    q = si.fp16_normal((int(cu[-1]), c.Hq, c.D), seed)
+    out = torch.full((int(cu[-1]), c.Hq, c.D), float("nan"), dtype=torch.float16, device=cuda_dev)
+    pkv.pf_paged_prefill_attention(c.pool, 0, dev(q, cuda_dev), c.bt_dev, c.lens_dev, dev(cu, cuda_dev), mx, scale,
+                                   out, workspace=ws)
+    torch.cuda.synchronize()
+    return q, cu, host(out)
+
+
+@pytest.mark.parametrize("hq,hkv,d,b,mx", [(12, 12, 64, 16, 8), (14, 2, 64, 1, 1), (8, 4, 128, 64, 4),
+                                           (40, 40, 128, 16, 8), (16, 2, 64, 256, 1), (6, 3, 64, 16, 4)])
+def test_short_append_on_the_decode_kernel(pkv, cuda_dev, oracle_mod, hq, hkv, d, b, mx):
+    lens = si.uniform_lengths(30, 1, 1500, seed=26)
+    rng = np.random.default_rng(7)
+    n_new = np.minimum(lens, rng.integers(0, mx + 1, size=lens.size)).astype(np.int32)
+    n_new[0] = min(mx, lens[0])
+    c = PagedCase(pkv, cuda_dev, lens, hq, hkv, d, b)
+    scale = 1.0 / np.sqrt(d)
+    q, cu, got = _run_ws(pkv, cuda_dev, c, n_new, scale)
+    ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, np.float32(scale))
+    assert_close_to_oracle(got, ref, what=f"append on the decode kernel {hq}/{hkv}x{d} B={b}")
+    # the same inputs through the kernel without a workspace
+    q2, cu2, got2 = _run(pkv, cuda_dev, c, n_new, scale)
+    assert_close_to_oracle(got2, ref, what="append on the prefill kernel")
+    assert pkv.pf_device_status(reset=True) == 0
+
+
+def test_one_new_token_on_the_decode_kernel_is_decode_bit_for_bit(pkv, cuda_dev):
+    lens = si.uniform_lengths(50, 1, 2000, seed=27)
+    c = PagedCase(pkv, cuda_dev, lens, 12, 12, 64, 16)
+    q, cu, got = _run_ws(pkv, cuda_dev, c, np.ones(lens.size, dtype=np.int32), 0.125)
+    dec = host(c.attention(0.125, q_dev=dev(q, cuda_dev)))
+    assert np.array_equal(got.view(np.uint16), dec.view(np.uint16))
+
+
+def test_short_append_large_batch(pkv, cuda_dev, oracle_mod):
+    """More than 1024 sequences: the kernel runs in two launches, and the
+    query rows are absolute in cu_q."""
+    lens = si.uniform_lengths(1500, 1, 120, seed=28)
+    rng = np.random.default_rng(8)
+    n_new = np.minimum(lens, rng.integers(0, 5, size=lens.size)).astype(np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 4, 4, 64, 16)
+    q, cu, got = _run_ws(pkv, cuda_dev, c, n_new, 0.125)
+    ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, 0.125)
+    assert_close_to_oracle(got, ref, what="append, 1500 sequences")
