@@ -24,8 +24,15 @@ std::mutex g_shape_mu;
 LaunchShape g_shapes[kMaxDevices][2][9][5];
 
 // kv-heads per work item: 4 (a 512 B run per token at head_dim 64), fewer
-// when the pool has fewer heads.
-int heads_per_item(int n_kv_heads) { return n_kv_heads >= 4 ? 4 : (n_kv_heads >= 2 ? 2 : 1); }
+// when the pool has fewer heads or a kv-head has many rows (q-heads, or
+// query tokens x q-heads): the consumer warps of a head then split its rows,
+// 2 each from 5 rows up and from 3 up with 2 heads.
+int heads_per_item(int n_kv_heads, int rows) {
+    int hg = n_kv_heads >= 4 ? 4 : (n_kv_heads >= 2 ? 2 : 1);
+    if (rows >= 5) hg = 1;
+    else if (rows >= 3 && hg > 2) hg = 2;
+    return hg;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static std::once_flag once;
@@ -41,14 +48,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-int encode_one(CUtensorMap *map, void *base, const pf_pool *pool) {
+int encode_one(CUtensorMap *map, void *base, const pf_pool *pool, int hg) {
     auto encode = get_encode_fn();
     if (!encode) return set_error(PF_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const uint64_t rows = (uint64_t)pool->n_layers * pool->n_blocks * pool->block_size;
     cuuint64_t dims[3] = {(cuuint64_t)pool->head_dim, (cuuint64_t)pool->n_kv_heads, (cuuint64_t)rows};
     cuuint64_t strides[2] = {(cuuint64_t)pool->head_dim * 2, (cuuint64_t)pool->n_kv_heads * pool->head_dim * 2};
     const int box_rows = pool->block_size < TB ? pool->block_size : TB;
-    const int hg = heads_per_item(pool->n_kv_heads);
     cuuint32_t box[3] = {(cuuint32_t)pool->head_dim, (cuuint32_t)hg, (cuuint32_t)box_rows};
     cuuint32_t estr[3] = {1u, 1u, 1u};
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
@@ -61,14 +67,16 @@ int encode_one(CUtensorMap *map, void *base, const pf_pool *pool) {
 
 }  // namespace
 
-int encode_pool_tmaps(pf_pool *pool, int device) {
+int encode_pool_tmaps(pf_pool *pool, int device, int hg, int *index) {
+    const int i = hg == 1 ? 0 : (hg == 2 ? 1 : 2);
+    *index = i;
     std::lock_guard<std::mutex> lock(pool->mu);
-    if (pool->tmap_ready[device]) return PF_OK;
-    int rc = encode_one(&pool->tmap_k[device], pool->k_base, pool);
+    if (pool->tmap_ready[device][i]) return PF_OK;
+    int rc = encode_one(&pool->tmap_k[device][i], pool->k_base, pool, hg);
     if (rc) return rc;
-    rc = encode_one(&pool->tmap_v[device], pool->v_base, pool);
+    rc = encode_one(&pool->tmap_v[device][i], pool->v_base, pool, hg);
     if (rc) return rc;
-    pool->tmap_ready[device] = true;
+    pool->tmap_ready[device][i] = true;
     return PF_OK;
 }
 
@@ -76,7 +84,7 @@ namespace {
 
 int kernel_for(const pf_pool *pool, int n_q_heads, KernelInfo *ki, int *hg) {
     const int G = n_q_heads / pool->n_kv_heads;
-    *hg = heads_per_item(pool->n_kv_heads);
+    *hg = heads_per_item(pool->n_kv_heads, G);
     *ki = pool->head_dim == 64 ? attn::kernel_d64(G, *hg) : attn::kernel_d128(G, *hg);
     if (!ki->fn || ki->smem == 0) return set_error(PF_ERR_UNSUPPORTED, "attention: unsupported head_dim / group");
     return PF_OK;
@@ -193,13 +201,14 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_error(e, "pf_paged_decode_attention: cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return set_error(PF_ERR_UNSUPPORTED, "device index out of range");
     pf_pool *pool = a.pool;
-    int rc = encode_pool_tmaps(pool, dev);
-    if (rc) return rc;
     int *status = device_status_ptr();
     if (!status) return PF_ERR_CUDA;
     KernelInfo ki;
     int HG = 0;
-    rc = kernel_for(pool, a.rows * pool->n_kv_heads, &ki, &HG);
+    int rc = kernel_for(pool, a.rows * pool->n_kv_heads, &ki, &HG);
+    if (rc) return rc;
+    int tmi = 0;
+    rc = encode_pool_tmaps(pool, dev, HG, &tmi);
     if (rc) return rc;
     const AttnPlan &plan = a.plan;
 
@@ -267,9 +276,9 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, ki.fn, pool->tmap_k[dev], pool->tmap_v[dev], p);
+            e = cudaLaunchKernelEx(&cfg, ki.fn, pool->tmap_k[dev][tmi], pool->tmap_v[dev][tmi], p);
         } else {
-            ki.fn<<<plan.grid, attn::NTHREADS, ki.smem, stream>>>(pool->tmap_k[dev], pool->tmap_v[dev], p);
+            ki.fn<<<plan.grid, attn::NTHREADS, ki.smem, stream>>>(pool->tmap_k[dev][tmi], pool->tmap_v[dev][tmi], p);
             e = cudaGetLastError();
         }
         if (e != cudaSuccess) return cuda_error(e, "pf_paged_decode_attention: launch");

@@ -566,32 +566,35 @@ __device__ __forceinline__ void store8(const Params &p, size_t o, const float (&
     }
 }
 
-// Normalise and store a whole pair's head from the state a warp holds:
-// lanes 0 .. D/8 - 1 hold dims [8 * lane, 8 * lane + 8) of acc.
-template <int D, int G>
-__device__ __forceinline__ void store_whole(const Params &p, const ItemDesc &d, int h, int lane, const float (&l)[G],
-                                            const float (&acc)[G][8]) {
+// Normalise and store the rows row0 .. row0 + R - 1 of a whole pair's head
+// from the state a warp holds: lanes 0 .. D/8 - 1 hold dims
+// [8 * lane, 8 * lane + 8) of acc.
+template <int D, int G, int R>
+__device__ __forceinline__ void store_whole(const Params &p, const ItemDesc &d, int h, int lane, int row0,
+                                            const float (&l)[R], const float (&acc)[R][8]) {
     constexpr int LPT = D / 8;
     if (lane < LPT) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int r = 0; r < R; ++r) {
+            const int g = row0 + r;
             const int i = g / p.gh;               // query token of row g
-            if (i >= d.nq) continue;
+            if (g >= G || i >= d.nq) continue;
             float x[8];
-            const float inv = 1.0f / l[g];
+            const float inv = 1.0f / l[r];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = acc[g][e] * inv;
+            for (int e = 0; e < 8; ++e) x[e] = acc[r][e] * inv;
             store8(p, ((size_t)(d.qrow0 + i) * p.n_q_heads + (size_t)h * p.gh + g - i * p.gh) * D + lane * 8, x);
         }
     }
 }
 
-// Record of one part of a cut pair for head hl (state as in store_whole,
-// m and l the same in every lane); the first part also writes the pair's job.
-template <int D, int G, int HG>
+// Rows row0 .. row0 + R - 1 of the record of one part of a cut pair for head
+// hl (state as in store_whole, m and l the same in every lane); the first
+// part also writes the pair's job.
+template <int D, int G, int HG, int R>
 __device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG> &sm, const ItemDesc &d, int hl,
-                                           int lane, bool write_job, const float (&m)[G], const float (&l)[G],
-                                           const float (&acc)[G][8]) {
+                                           int lane, int row0, bool write_job, const float (&m)[R],
+                                           const float (&l)[R], const float (&acc)[R][8]) {
     constexpr int LPT = D / 8;
     constexpr int REC = G * (D + 2);
     const int Hkv = p.n_kv_heads;
@@ -599,14 +602,16 @@ __device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG>
     float *part = p.partials + rec * REC;
     if (lane < LPT) {
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int r = 0; r < R; ++r) {
+            const int g = row0 + r;
+            if (g >= G) continue;
             // rows of D + 2 floats keep 8-float runs 8-byte (not 16-byte) aligned
             float2 *d2 = reinterpret_cast<float2 *>(part + g * (D + 2) + lane * 8);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) d2[i] = make_float2(acc[g][2 * i], acc[g][2 * i + 1]);
+            for (int i = 0; i < 4; ++i) d2[i] = make_float2(acc[r][2 * i], acc[r][2 * i + 1]);
             if (lane == 0) {
-                part[g * (D + 2) + D] = m[g];
-                part[g * (D + 2) + D + 1] = l[g];
+                part[g * (D + 2) + D] = m[r];
+                part[g * (D + 2) + D + 1] = l[r];
             }
         }
     }
@@ -711,13 +716,21 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
     constexpr int WPH = Shape<D, HG>::WPH;
     constexpr int LPT = D / 8;        // lanes per token row
     constexpr int TPW = 32 / LPT;     // tokens per warp-step
-    constexpr int TPT = TB / WPH;     // tokens of a tile this warp serves
+    // Several warps of a head split its rows when it has at least as many
+    // rows as warps (each then holds fewer of them: registers, occupancy);
+    // otherwise they split each tile's tokens and merge at the end.
+    constexpr bool RSPLIT = WPH > 1 && G >= WPH;
+    constexpr int R = RSPLIT ? (G + WPH - 1) / WPH : G;   // rows this warp holds
+    constexpr int ARRIVE = RSPLIT ? WPH : 1;             // a cut part's arrivals per head
+    constexpr int TPT = RSPLIT ? TB : TB / WPH;          // tokens of a tile this warp serves
     constexpr int STEPS = TPT / TPW;
     static_assert(STEPS * TPW == TPT, "tile must split into whole warp-steps");
     const int grp = lane / LPT;
     const int sub = lane % LPT;
     const int hl = cw / WPH;          // head within the group
-    const int part = cw % WPH;        // which share of each tile's tokens
+    const int part = cw % WPH;        // which share of the head's rows, or of each tile's tokens
+    const int row0 = RSPLIT ? part * R : 0;
+    const int tok_base = RSPLIT ? 0 : part * TPT;
     const int Hq = p.n_q_heads;
 
     // (as in the producer: the previous kernel may still be writing `out`)
@@ -758,20 +771,20 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                     if (pending & 1) {
                         const PendPart &pp = sm.pend[cw][0];
                         got0 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pp.first * HG + hl,
-                                                      (unsigned)(pp.n_parts - 1));
+                                                      (unsigned)(pp.n_parts * ARRIVE - 1));
                     }
                     if (pending & 2) {
                         const PendPart &pp = sm.pend[cw][1];
                         got1 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pp.first * HG + hl,
-                                                      (unsigned)(pp.n_parts - 1));
+                                                      (unsigned)(pp.n_parts * ARRIVE - 1));
                     }
                 }
                 got0 = __shfl_sync(FULL, got0, 0);
                 got1 = __shfl_sync(FULL, got1, 0);
                 const PendPart pp0 = sm.pend[cw][0];
                 const PendPart pp1 = sm.pend[cw][1];
-                const bool last0 = (pending & 1) && got0 == (unsigned)(pp0.n_parts - 1);
-                const bool last1 = (pending & 2) && got1 == (unsigned)(pp1.n_parts - 1);
+                const bool last0 = (pending & 1) && got0 == (unsigned)(pp0.n_parts * ARRIVE - 1);
+                const bool last1 = (pending & 2) && got1 == (unsigned)(pp1.n_parts * ARRIVE - 1);
                 if (last0 || last1) {
                     if (lane == 0) fence_acq_rel_gpu();
                     __syncwarp();
@@ -788,22 +801,24 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
         const int h = d.h0 + hl;
         const bool active = h < p.n_kv_heads;   // ragged last group: idle warps keep the protocol
 
-        // Row g of the head: query token g / gh, q-head g % gh; it sees
-        // tokens 0 .. lim[g] (L - 1 for decode; causal for an append).
-        float qf[G][8];
-        int lim[G];
+        // This warp holds rows row0 .. row0 + R - 1 of the head.  Row g:
+        // query token g / gh, q-head g % gh; it sees tokens 0 .. lim (L - 1
+        // for decode; causal for an append).
+        float qf[R][8];
+        int lim[R];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int r = 0; r < R; ++r) {
+            const int g = row0 + r;
             const int i = g / p.gh;
-            const bool valid = active && i < d.nq;
-            lim[g] = valid ? d.L - d.nq + i : -1;
+            const bool valid = active && g < G && i < d.nq;
+            lim[r] = valid ? d.L - d.nq + i : -1;
             if (valid) {
                 const uint4 raw = *reinterpret_cast<const uint4 *>(
                     &sm.q[slot][((i * HG + hl) * p.gh + g - i * p.gh) * D + sub * 8]);
-                half8_to_float(raw, qf[g]);
+                half8_to_float(raw, qf[r]);
             }
 #pragma unroll
-            for (int e = 0; e < 8; ++e) qf[g][e] = valid ? qf[g][e] * p.scale_log2 : 0.0f;
+            for (int e = 0; e < 8; ++e) qf[r][e] = valid ? qf[r][e] * p.scale_log2 : 0.0f;
         }
         // Fused decode step: the new token's rows stand in for the tile's row
         // L - 1 (whatever the tile read there), and the first warp of each
@@ -822,9 +837,9 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(&sm.qempty[slot]));
 
-        float m[G], l[G], acc[G][8];
+        float m[R], l[R], acc[R][8];
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
+        for (int g = 0; g < R; ++g) {
             m[g] = -INFINITY;
             l[g] = 0.0f;
 #pragma unroll
@@ -848,16 +863,16 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
 #pragma unroll
                 for (int step = 0; step < STEPS; ++step) {
                     kraw[step] = *reinterpret_cast<const uint4 *>(
-                        kt + ((part * TPT + step * TPW + grp) * HG + hl) * D + sub * 8);
-                    if (part * TPT + step * TPW + grp == newr) kraw[step] = nk;
+                        kt + ((tok_base + step * TPW + grp) * HG + hl) * D + sub * 8);
+                    if (tok_base + step * TPW + grp == newr) kraw[step] = nk;
                 }
-                float z[STEPS][G];
+                float z[STEPS][R];
 #pragma unroll
                 for (int step = 0; step < STEPS; ++step) {
                     float kf[8];
                     half8_to_float(kraw[step], kf);
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
+                    for (int g = 0; g < R; ++g) {
                         float a = 0.0f;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) a = fmaf(qf[g][i], kf[i], a);
@@ -869,15 +884,15 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
 #pragma unroll
                     for (int step = 0; step < STEPS; ++step) {
 #pragma unroll
-                        for (int g = 0; g < G; ++g) z[step][g] += __shfl_xor_sync(FULL, z[step][g], o);
+                        for (int g = 0; g < R; ++g) z[step][g] += __shfl_xor_sync(FULL, z[step][g], o);
                     }
                 }
                 if (masked) {
 #pragma unroll
                     for (int step = 0; step < STEPS; ++step) {
-                        const int tok = tile0 + part * TPT + step * TPW + grp;
+                        const int tok = tile0 + tok_base + step * TPW + grp;
 #pragma unroll
-                        for (int g = 0; g < G; ++g)
+                        for (int g = 0; g < R; ++g)
                             if (tok > lim[g]) z[step][g] = -INFINITY;
                     }
                 }
@@ -885,7 +900,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 // maximum m (the same in every lane) is raised only when the
                 // tile passes it by more than 2^8
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < R; ++g) {
                     float mt = z[0][g];
 #pragma unroll
                     for (int step = 1; step < STEPS; ++step) mt = fmaxf(mt, z[step][g]);
@@ -904,19 +919,19 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
 #pragma unroll
                 for (int step = 0; step < STEPS; ++step) {
                     vraw[step] = *reinterpret_cast<const uint4 *>(
-                        vt + ((part * TPT + step * TPW + grp) * HG + hl) * D + sub * 8);
-                    if (part * TPT + step * TPW + grp == newr) vraw[step] = nvv;
+                        vt + ((tok_base + step * TPW + grp) * HG + hl) * D + sub * 8);
+                    if (tok_base + step * TPW + grp == newr) vraw[step] = nvv;
                 }
 #pragma unroll
                 for (int step = 0; step < STEPS; ++step) {
                     float vf[8];
                     half8_to_float(vraw[step], vf);
-                    if (masked && tile0 + part * TPT + step * TPW + grp >= d.L) {
+                    if (masked && tile0 + tok_base + step * TPW + grp >= d.L) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) vf[i] = 0.0f;   // tail rows may hold anything
                     }
 #pragma unroll
-                    for (int g = 0; g < G; ++g) {
+                    for (int g = 0; g < R; ++g) {
                         // a masked score has weight 0 (also when m is still -inf)
                         const float pz = (masked && z[step][g] == -INFINITY) ? 0.0f : exp2f(z[step][g] - m[g]);
                         l[g] += pz;
@@ -933,19 +948,19 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
 #pragma unroll
         for (int o = LPT; o < 32; o <<= 1) {
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
+            for (int g = 0; g < R; ++g) {
                 l[g] += __shfl_xor_sync(FULL, l[g], o);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[g][i] += __shfl_xor_sync(FULL, acc[g][i], o);
             }
         }
 
-        if constexpr (WPH > 1) {
+        if constexpr (WPH > 1 && !RSPLIT) {
             // The WPH warps of a head meet in shared memory; the first of
             // them carries the merged state on.
             if (lane < LPT) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < R; ++g) {
 #pragma unroll
                     for (int i = 0; i < 8; ++i) sm.red[cw][g][lane * 8 + i] = acc[g][i];
                     if (lane == 0) {
@@ -957,7 +972,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
             if (!warps_sync(cbar, cphase, p.status, lane)) return;
             if (part == 0) {
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
+                for (int g = 0; g < R; ++g) {
                     float mx = -INFINITY;
 #pragma unroll
                     for (int w = 0; w < WPH; ++w) mx = fmaxf(mx, sm.red[cw + w][g][D]);
@@ -983,19 +998,19 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
             }
             if (!warps_sync(cbar, cphase, p.status, lane)) return;   // red[] is reused next item
         }
-        const bool leader = part == 0 && active;
+        const bool leader = (RSPLIT || part == 0) && active;
         if (d.kind == kWhole) {
-            if (leader) store_whole<D, G>(p, d, h, lane, l, acc);
+            if (leader) store_whole<D, G, R>(p, d, h, lane, row0, l, acc);
         } else if (leader) {
             if (d.kind == kChunk) {
                 // chunk 0 of the sequence also writes the merge job
-                write_part<D, G, HG>(p, sm, d, hl, lane, d.b == 0 && hl == 0, m, l, acc);
+                write_part<D, G, HG, R>(p, sm, d, hl, lane, row0, d.b == 0 && hl == 0 && part == 0, m, l, acc);
             } else {
                 // Span part: write the record and note the pair; it is
                 // counted when this CTA has no items left.  The pair's parts
                 // are spans owner(a) .. owner(a + b - 1); the first uses
                 // slot 1 when the pair starts inside it.
-                write_part<D, G, HG>(p, sm, d, hl, lane, false, m, l, acc);
+                write_part<D, G, HG, R>(p, sm, d, hl, lane, row0, false, m, l, acc);
                 if (lane == 0) {
                     // units a .. a + b - 1: the cost unit, then the tiles
                     const SpanMap map((long long)sm.pre[p.n_seqs] * p.n_groups, gridDim.x);
@@ -1098,7 +1113,9 @@ __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const C
 // get all the registers they ask for.
 template <int D, int G, int HG>
 struct RegisterCap {
-    static constexpr bool k128 = D == 64 && (G <= 2 || (HG <= 2 && G <= 3));
+    static constexpr int WPH = Shape<D, HG>::WPH;
+    static constexpr int ROWS = (WPH > 1 && G >= WPH) ? (G + WPH - 1) / WPH : G;   // rows per consumer warp
+    static constexpr bool k128 = D == 64 && (ROWS <= 2 || (HG <= 2 && G <= 3));
 };
 
 template <int D, int G, int HG>
