@@ -492,6 +492,28 @@ def run_ours(args, dist):
     pr_flops = 4.0 * Hq * D * Sp * Lp * (Lp + 1) / 2        # q.k and p.v over every causal pair
     del q_app, o_app, q_pr, o_pr
 
+    # grouped heads: 14 q-heads over 2 kv-heads x 64, 256 sequences of
+    # U[32, 4096] tokens (each K/V byte serves 7 q-heads), attention alone
+    wg = si.WORKLOADS["gqa"]
+    g_lens = si.uniform_lengths(wg["n_seqs"], wg["len_lo"], wg["len_hi"], seed=12)
+    gHq, gHkv, gD, gB = wg["n_q_heads"], wg["n_kv_heads"], wg["head_dim"], 16
+    gN = int(sum(-(-int(L_) // gB) for L_ in g_lens)) + 64
+    g_maxb = -(-int(g_lens.max()) // gB)
+    g_bt = to(si.block_tables(g_lens, gB, gN, si.SEED_SHUFFLE, max_blocks=g_maxb))
+    g_lens_d = to(g_lens)
+    g_reps = []
+    for r in range(2):
+        gk = torch.empty((1, gN, gB, gHkv, gD), dtype=torch.float16, device=device).normal_()
+        gv = torch.empty_like(gk).normal_()
+        gpool = pkv.pf_pool_create(gk, gv)
+        gq = torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device).normal_()
+        g_reps.append((gk, gv, gpool, gq, torch.empty_like(gq), pkv.make_workspace(gpool, wg["n_seqs"], gHq, g_maxb)))
+    g_args = [(gr[2].handle, 0, P(gr[3]), P(g_bt), g_maxb, P(g_lens_d), wg["n_seqs"], gHq, ctypes.c_float(wg["scale"]),
+               P(gr[4]), pkv.PF_F16, 0, P(gr[5]), gr[5].numel(), sp) for gr in g_reps]
+    gqa_ms = time_calls(lambda i: check(lib.pf_paged_decode_attention(*g_args[i % 2])), Kg)
+    gqa_bytes = attention_bytes(g_lens, gHq, gHkv, gD, gB)
+    del g_reps
+
     clocks = sampler.stop()
     fp32_peak = props.multi_processor_count * 128 * 2 * (clocks.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
     status = pkv.pf_device_status(reset=True)
@@ -607,6 +629,10 @@ def run_ours(args, dist):
                            "fp32_fma_peak_tflops": round(fp32_peak, 1),
                            "frac": round(pr_flops / (pr_ms / 1e3) / 1e12 / fp32_peak, 4),
                            "peak_note": "SMs x 128 fp32 lanes x 2 flop x max SM clock (CUDA cores, no tensor cores)"},
+        "gqa_attention": {"workload": "256 sequences of U[32,4096] tokens, 14 q-heads / 2 kv-heads x 64, "
+                                      "block 16, shuffled frames", "ms": round(gqa_ms, 5), "bytes": gqa_bytes,
+                          "gbs": round(gqa_bytes / (gqa_ms / 1e3) / 1e9, 1),
+                          "frac_of_measured_copy": round(gqa_bytes / (gqa_ms / 1e3) / 1e9 / peak, 4)},
         "gather": {"gbs": round(g_bytes / (gather_ms / 1e3) / 1e9, 1), "ms": round(gather_ms, 5),
                    "bytes": g_bytes, "frac_of_measured_copy": round(g_bytes / (gather_ms / 1e3) / 1e9 / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
