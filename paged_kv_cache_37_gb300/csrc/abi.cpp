@@ -92,7 +92,7 @@ int pf_pool_create(pf_pool **out, void *k_base, void *v_base, int n_layers, int 
     p->head_dim = head_dim;
     p->dtype = dtype;
     for (int i = 0; i < pkv::kMaxDevices; ++i)
-        for (int j = 0; j < 3; ++j) p->tmap_ready[i][j] = false;
+        for (int j = 0; j < 4; ++j) p->tmap_ready[i][j] = false;
     *out = p;
     return PF_OK;
 }
@@ -244,9 +244,10 @@ static int decode_call(const pf_pool *pool, int layer, const void *q, const void
         return pkv::set_error(PF_ERR_INVALID,
                               "pf_paged_decode_attention: n_q_heads must be a positive multiple of n_kv_heads");
     int group = n_q_heads / pool->n_kv_heads;
-    if (group > 8)
+    if (group > 16 || (group > 8 && (split_tokens != 0 || pool->block_size < 16)))
         return pkv::set_error(PF_ERR_UNSUPPORTED,
-                              "pf_paged_decode_attention: at most 8 q-heads per kv-head are built");
+                              "pf_paged_decode_attention: at most 8 q-heads per kv-head are built (16 with "
+                              "split_tokens = 0 and pages of at least 16 tokens)");
     if (max_blocks_per_seq <= 0)
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_decode_attention: max_blocks_per_seq must be positive");
     if (!(scale > 0.0f) || scale != scale)

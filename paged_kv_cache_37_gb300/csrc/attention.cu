@@ -21,7 +21,41 @@ struct LaunchShape {
 };
 
 std::mutex g_shape_mu;
-LaunchShape g_shapes[kMaxDevices][2][9][5];
+LaunchShape g_shapes[kMaxDevices][2][17][5][2];
+
+// Kv-heads with at least this many rows (q-heads, or query tokens x
+// q-heads) take the tensor-core consumers when the call runs the span
+// schedule over pages of at least TB tokens.  Measured (256 sequences of
+// U[32, 4096] tokens, GB/s, tensor-core vs CUDA-core consumers): head_dim 64,
+// 2 rows 3013 vs 4088, 3 rows 2988 vs 2402, 4 rows 2976 vs 2462, 8 rows 2404
+// vs 1132; head_dim 128, 2 rows 3905 vs 2585, 8 rows 3573 vs 867.
+#ifndef PKV_MMA_MIN_ROWS_D64
+#define PKV_MMA_MIN_ROWS_D64 3
+#endif
+#ifndef PKV_MMA_MIN_ROWS_D128
+#define PKV_MMA_MIN_ROWS_D128 2
+#endif
+constexpr int kMmaMaxRows = 16;
+int mma_min_rows(int head_dim) { return head_dim == 64 ? PKV_MMA_MIN_ROWS_D64 : PKV_MMA_MIN_ROWS_D128; }
+
+// kv-heads per item of the tensor-core consumers: as many as the pool has,
+// up to PKV_MMA_MAX_HEADS (the boxes of a token's heads are issued back to
+// back, so more heads read longer runs of each page row), 2 at head_dim 128
+// above 8 rows (shared memory).
+#ifndef PKV_MMA_MAX_HEADS
+#define PKV_MMA_MAX_HEADS 4
+#endif
+int mma_heads(int n_kv_heads, int rows, int head_dim) {
+    int hg = n_kv_heads >= 4 ? 4 : (n_kv_heads >= 2 ? 2 : 1);
+    if (hg > PKV_MMA_MAX_HEADS) hg = PKV_MMA_MAX_HEADS;
+    if (head_dim == 128 && rows > 8 && hg > 2) hg = 2;
+    return hg;
+}
+
+KernelInfo kernel_mma(int head_dim, int rows, int hg) {
+    if (head_dim == 64) return rows <= 8 ? attn::kernel_mma_d64_s(rows, hg) : attn::kernel_mma_d64_l(rows, hg);
+    return rows <= 8 ? attn::kernel_mma_d128_s(rows, hg) : attn::kernel_mma_d128_l(rows, hg);
+}
 
 // kv-heads per work item: 4 (a 512 B run per token at head_dim 64), fewer
 // when the pool has fewer heads or a kv-head has many rows (q-heads, or
@@ -48,18 +82,34 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
+// hg > 0: boxes {D, hg heads, TB rows}, unswizzled.  hg == 0: the
+// tensor-core layout, one head, 64-element halves of a row swizzled in
+// 128-byte rows: {64, TB} boxes of a 3-D map at head_dim 64, of a 4-D map
+// {64, D / 64, heads, rows} at head_dim 128.
 int encode_one(CUtensorMap *map, void *base, const pf_pool *pool, int hg) {
     auto encode = get_encode_fn();
     if (!encode) return set_error(PF_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const uint64_t rows = (uint64_t)pool->n_layers * pool->n_blocks * pool->block_size;
-    cuuint64_t dims[3] = {(cuuint64_t)pool->head_dim, (cuuint64_t)pool->n_kv_heads, (cuuint64_t)rows};
-    cuuint64_t strides[2] = {(cuuint64_t)pool->head_dim * 2, (cuuint64_t)pool->n_kv_heads * pool->head_dim * 2};
+    const cuuint64_t D = (cuuint64_t)pool->head_dim;
+    const cuuint64_t H = (cuuint64_t)pool->n_kv_heads;
     const int box_rows = pool->block_size < TB ? pool->block_size : TB;
-    cuuint32_t box[3] = {(cuuint32_t)pool->head_dim, (cuuint32_t)hg, (cuuint32_t)box_rows};
-    cuuint32_t estr[3] = {1u, 1u, 1u};
-    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    CUresult r;
+    if (hg > 0 || D == 64) {
+        cuuint64_t dims[3] = {D, H, (cuuint64_t)rows};
+        cuuint64_t strides[2] = {D * 2, H * D * 2};
+        cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)(hg > 0 ? hg : 1), (cuuint32_t)box_rows};
+        r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, hg > 0 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        cuuint64_t dims[4] = {64, D / 64, H, (cuuint64_t)rows};
+        cuuint64_t strides[3] = {128, D * 2, H * D * 2};
+        cuuint32_t box[4] = {64u, 1u, 1u, (cuuint32_t)box_rows};
+        r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (r != CUDA_SUCCESS)
         return set_error(PF_ERR_CUDA, "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r));
     return PF_OK;
@@ -68,7 +118,7 @@ int encode_one(CUtensorMap *map, void *base, const pf_pool *pool, int hg) {
 }  // namespace
 
 int encode_pool_tmaps(pf_pool *pool, int device, int hg, int *index) {
-    const int i = hg == 1 ? 0 : (hg == 2 ? 1 : 2);
+    const int i = hg == 0 ? 3 : (hg == 1 ? 0 : (hg == 2 ? 1 : 2));
     *index = i;
     std::lock_guard<std::mutex> lock(pool->mu);
     if (pool->tmap_ready[device][i]) return PF_OK;
@@ -82,19 +132,29 @@ int encode_pool_tmaps(pf_pool *pool, int device, int hg, int *index) {
 
 namespace {
 
-int kernel_for(const pf_pool *pool, int n_q_heads, KernelInfo *ki, int *hg) {
+// The kernel for G = n_q_heads / n_kv_heads rows per kv-head: *hg its
+// kv-heads per item, *mma whether it has the tensor-core consumers (one
+// kv-head per item, its tensor map the swizzled one).
+int kernel_for(const pf_pool *pool, int n_q_heads, bool spans, KernelInfo *ki, int *hg, bool *mma) {
     const int G = n_q_heads / pool->n_kv_heads;
-    *hg = heads_per_item(pool->n_kv_heads, G);
-    *ki = pool->head_dim == 64 ? attn::kernel_d64(G, *hg) : attn::kernel_d128(G, *hg);
+    *mma = spans && pool->block_size >= TB && G >= mma_min_rows(pool->head_dim) && G <= kMmaMaxRows;
+    if (*mma) {
+        *hg = mma_heads(pool->n_kv_heads, G, pool->head_dim);
+        *ki = kernel_mma(pool->head_dim, G, *hg);
+    } else {
+        *hg = heads_per_item(pool->n_kv_heads, G);
+        *ki = pool->head_dim == 64 ? attn::kernel_d64(G, *hg) : attn::kernel_d128(G, *hg);
+    }
     if (!ki->fn || ki->smem == 0) return set_error(PF_ERR_UNSUPPORTED, "attention: unsupported head_dim / group");
     return PF_OK;
 }
 
 // Persistent grid of the kernel on the current device: SMs x resident CTAs.
-int resident_grid(const pf_pool *pool, int n_q_heads, int *grid) {
+int resident_grid(const pf_pool *pool, int n_q_heads, bool spans, int *grid) {
     KernelInfo ki;
     int HG = 0;
-    int rc = kernel_for(pool, n_q_heads, &ki, &HG);
+    bool mma = false;
+    int rc = kernel_for(pool, n_q_heads, spans, &ki, &HG, &mma);
     if (rc) return rc;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -103,7 +163,7 @@ int resident_grid(const pf_pool *pool, int n_q_heads, int *grid) {
     const int D = pool->head_dim;
     const int G = n_q_heads / pool->n_kv_heads;
     std::lock_guard<std::mutex> lock(g_shape_mu);
-    LaunchShape &sh = g_shapes[dev][D == 64 ? 0 : 1][G][HG];
+    LaunchShape &sh = g_shapes[dev][D == 64 ? 0 : 1][G][HG][mma ? 1 : 0];
     if (!sh.ready) {
         const void *fn_ptr = reinterpret_cast<const void *>(ki.fn);
         e = cudaFuncSetAttribute(fn_ptr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ki.smem);
@@ -147,15 +207,15 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
         return set_error(PF_ERR_INVALID, "attention: split_tokens must be -1, 0 or positive");
     KernelInfo ki;
     int HG = 0;
-    int rc = kernel_for(pool, n_q_heads, &ki, &HG);
-    if (rc) return rc;
-    const int G = n_q_heads / pool->n_kv_heads;
-    const size_t rec_bytes = (size_t)G * (size_t)(pool->head_dim + 2) * sizeof(float);
-    const int per_launch = n_seqs < attn::kMaxSeqsPerLaunch ? n_seqs : attn::kMaxSeqsPerLaunch;
+    bool mma = false;
     plan->spans = split_tokens == 0;
+    int rc = kernel_for(pool, n_q_heads, plan->spans, &ki, &HG, &mma);
+    if (rc) return rc;
+    const size_t rec_bytes = (size_t)ki.rows * (size_t)(pool->head_dim + 2) * sizeof(float);
+    const int per_launch = n_seqs < attn::kMaxSeqsPerLaunch ? n_seqs : attn::kMaxSeqsPerLaunch;
     plan->grid = 0;
     if (need_device) {
-        rc = resident_grid(pool, n_q_heads, &plan->grid);
+        rc = resident_grid(pool, n_q_heads, plan->spans, &plan->grid);
         if (rc) return rc;
     }
     // [reserved: 256 B][fp32 records][arrival counters][merge jobs]
@@ -165,7 +225,7 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
     if (plan->spans) {
         plan->chunk = TB;
         int grid = plan->grid;
-        if (!need_device && resident_grid(pool, n_q_heads, &grid) != PF_OK) {
+        if (!need_device && resident_grid(pool, n_q_heads, true, &grid) != PF_OK) {
             clear_error();
             grid = kGridBoundNoDevice;
         }
@@ -203,14 +263,15 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     pf_pool *pool = a.pool;
     int *status = device_status_ptr();
     if (!status) return PF_ERR_CUDA;
+    const AttnPlan &plan = a.plan;
     KernelInfo ki;
     int HG = 0;
-    int rc = kernel_for(pool, a.rows * pool->n_kv_heads, &ki, &HG);
+    bool mma = false;
+    int rc = kernel_for(pool, a.rows * pool->n_kv_heads, plan.spans, &ki, &HG, &mma);
     if (rc) return rc;
     int tmi = 0;
-    rc = encode_pool_tmaps(pool, dev, HG, &tmi);
+    rc = encode_pool_tmaps(pool, dev, mma ? 0 : HG, &tmi);
     if (rc) return rc;
-    const AttnPlan &plan = a.plan;
 
     attn::Params p;
     p.k_pool = static_cast<__half *>(pool->k_base);
@@ -240,6 +301,7 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     // 2 us more than 4.
     p.prefetch_tiles = a.overlap_previous ? 16 : 4;
     p.gh = a.n_q_heads / pool->n_kv_heads;
+    p.rows = a.rows;
     const size_t out_elem = a.out_dtype == PF_F32 ? 4 : 2;
     const size_t row = (size_t)a.n_q_heads * pool->head_dim;   // q / out elements per sequence
 

@@ -152,7 +152,8 @@ struct Params {
     // attending causally.  Null for decode (one query per sequence, row s).
     // A kv-head's G rows are its query tokens x its gh q-heads.
     const int32_t *cu_q;
-    int gh;               // q-heads per kv-head (G for decode)
+    int gh;               // q-heads per kv-head
+    int rows;             // rows per kv-head the call allows (gh for decode; <= the instance's G)
 };
 
 // Span map of the span schedule: the W flattened tiles cut into
@@ -181,14 +182,32 @@ struct Shape {
     static constexpr int WPH = NCW / HG;      // consumer warps per head
 };
 
+// Tensor-core consumers (HG kv-heads per item, each head's tiles dealt
+// round-robin to its NCW / HG consumer warps): the ring takes what is left
+// of a CTA's share of the SM's 228 KB -- 3 CTAs per SM at head_dim 64, 2 at
+// 128 -- after the fixed part (q slots, new rows, the warps' merge area, the
+// span tables, barriers), between 2 and 16 stages.
 template <int D, int G, int HG>
+struct MmaShape {
+    static constexpr int STAGE_BYTES = 2 * TB * HG * D * 2;
+    static constexpr int BUDGET = (D == 64 ? 228 * 1024 / 3 : 228 * 1024 / 2) - 2048;   // reserved + alignment slack
+    static constexpr int FIXED = NQ * HG * G * D * 2 + NQ * 2 * HG * D * 2 + NCW * G * (D + 2) * 4 +
+                                 (kMaxSeqsPerLaunch + 1) * 4 + kMaxSeqsPerLaunch + 2048;
+    static constexpr int NS_RAW = (BUDGET - FIXED) / STAGE_BYTES;
+    static constexpr int NS = NS_RAW < 2 ? 2 : (NS_RAW > 16 ? 16 : NS_RAW);
+};
+
+// MMA: the stages hold swizzled tiles (128-byte rows, 16-byte chunks XORed
+// with the row index mod 8) and must sit at 1024-byte boundaries; the kernel
+// places the struct there at run time.
+template <int D, int G, int HG, bool MMA = false>
 struct __align__(128) Smem {
-    static constexpr int NS = Shape<D, HG>::NS;
+    static constexpr int NS = MMA ? MmaShape<D, G, HG>::NS : Shape<D, HG>::NS;
     __half k[NS][Shape<D, HG>::STAGE_HALVES];
     __half v[NS][Shape<D, HG>::STAGE_HALVES];
     __half q[NQ][HG * G * D];
     __half knew[NQ][2][HG * D];   // fused step: the new token's K and V rows of the item's heads
-    float red[Shape<D, HG>::WPH > 1 ? NCW : 1][G][D + 2];   // per consumer warp: acc[D], m, l
+    float red[(MMA || Shape<D, HG>::WPH > 1) ? NCW : 1][G][D + 2];   // per consumer warp: acc[D], m, l
     ItemDesc desc[NQ];
     uint64_t full[NS];
     uint64_t empty[NS];
@@ -227,12 +246,12 @@ __device__ __forceinline__ void prefetch_table_rows(const Params &p) {
 }
 
 // Append: a sequence without query tokens has no work (length 0); more
-// query tokens than its length or than the G rows hold is flagged (and
+// query tokens than its length or than the call's rows hold is flagged (and
 // clamped where the tokens are read).  Decode: the length as is.
-__device__ __forceinline__ int append_length(const Params &p, int s, int L, int G) {
+__device__ __forceinline__ int append_length(const Params &p, int s, int L) {
     if (p.cu_q == nullptr) return L;
     const int nq = p.cu_q[s + 1] - p.cu_q[s];
-    if (nq < 0 || nq > L || nq * p.gh > G) atomicOr(p.status, PF_DEV_BAD_LENGTH);
+    if (nq < 0 || nq > L || nq * p.gh > p.rows) atomicOr(p.status, PF_DEV_BAD_LENGTH);
     return nq > 0 ? L : 0;
 }
 
@@ -246,10 +265,49 @@ struct ProdItem {
     int qrow0, nq;    // q row of the sequence's first query token; its query tokens
 };
 
-template <int D, int G, int HG>
+// Issue one K or V tile (pool rows r .. r + TB - 1 of heads h0 ..) into a
+// stage.  Plain: one box {D, HG, TB}.  MMA: per head and 64-element half of
+// the head, one swizzled box {64, TB} to stage offset (head * D / 64 + half)
+// * TB * 64; the boxes of a token's heads are issued back to back, so a page
+// row is still read as one run.
+template <int D, int HG, bool MMA>
+__device__ __forceinline__ void tile_load(__half *dst, const CUtensorMap *map, int h0, int r, uint32_t bar,
+                                          uint64_t pol) {
+    if constexpr (!MMA) {
+        tma_load_3d(smem_addr(dst), map, 0, h0, r, bar, pol);
+    } else {
+#pragma unroll
+        for (int hl = 0; hl < HG; ++hl) {
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf) {
+                const uint32_t a = smem_addr(dst + (hl * (D / 64) + hf) * TB * 64);
+                if constexpr (D == 64) tma_load_3d(a, map, 0, h0 + hl, r, bar, pol);
+                else tma_load_4d(a, map, 0, hf, h0 + hl, r, bar, pol);
+            }
+        }
+    }
+}
+
+template <int D, int HG, bool MMA>
+__device__ __forceinline__ void tile_prefetch(const CUtensorMap *map, int h0, int r) {
+    if constexpr (!MMA) {
+        tma_prefetch_3d(map, 0, h0, r);
+    } else {
+#pragma unroll
+        for (int hl = 0; hl < HG; ++hl) {
+#pragma unroll
+            for (int hf = 0; hf < D / 64; ++hf) {
+                if constexpr (D == 64) tma_prefetch_3d(map, 0, h0 + hl, r);
+                else tma_prefetch_4d(map, 0, hf, h0 + hl, r);
+            }
+        }
+    }
+}
+
+template <int D, int G, int HG, bool MMA = false>
 __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorMap *tmv, const Params &p,
-                                         Smem<D, G, HG> &sm, int lane) {
-    constexpr int NS = Shape<D, HG>::NS;
+                                         Smem<D, G, HG, MMA> &sm, int lane) {
+    constexpr int NS = Smem<D, G, HG, MMA>::NS;
     const uint64_t pol = policy_evict_first();
     const int B = p.block_size;
     const int C = p.chunk;
@@ -283,7 +341,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         // flagged them); decode: one, at row s.
         if (p.cu_q != nullptr) {
             it.qrow0 = p.cu_q[it.s];
-            it.nq = max(1, min(min(p.cu_q[it.s + 1] - it.qrow0, L), G / p.gh));
+            it.nq = max(1, min(min(p.cu_q[it.s + 1] - it.qrow0, L), p.rows / p.gh));
         } else {
             it.qrow0 = it.s;
             it.nq = 1;
@@ -303,7 +361,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
                 atomicOr(p.status, PF_DEV_BAD_LENGTH);
                 L = L < 0 ? 0 : maxctx;
             }
-            L = append_length(p, s, L, G);
+            L = append_length(p, s, L);
         }
         wl = L;
         wu = (L + C - 1) / C;
@@ -418,8 +476,8 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         const int id = __shfl_sync(FULL, it.ids0, pa);
         if (j < p.prefetch_tiles && j < tiles0 && id >= 0 && id < p.n_blocks) {
             const int r = p.layer_row0 + id * B + (t % B);
-            tma_prefetch_3d(tmk, 0, it.h0, r);
-            tma_prefetch_3d(tmv, 0, it.h0, r);
+            tile_prefetch<D, HG, MMA>(tmk, it.h0, r);
+            tile_prefetch<D, HG, MMA>(tmv, it.h0, r);
         }
     }
     // Launched as a programmatic dependent: wait for the previous kernel on
@@ -514,10 +572,10 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
                 if (lane == 0) {
                     mbar_arrive_expect_tx(full_bar, kTileBytes);
                     const int r = p.layer_row0 + id * B + (t % B);
-                    tma_load_3d(smem_addr(sm.k[stage]), tmk, 0, it.h0, r, full_bar, pol);
-                    tma_load_3d(smem_addr(sm.v[stage]), tmv, 0, it.h0, r, full_bar, pol);
+                    tile_load<D, HG, MMA>(sm.k[stage], tmk, it.h0, r, full_bar, pol);
+                    tile_load<D, HG, MMA>(sm.v[stage], tmv, it.h0, r, full_bar, pol);
                 }
-            } else {
+            } else if constexpr (!MMA) {
                 // B < TB (B = 1): one box of B rows per page
                 const int pb = (t + nt - 1) / B - it.pg0;
                 const int np = pb - pa + 1;
@@ -710,6 +768,83 @@ __device__ __forceinline__ void merge_pair(const Params &p, int kind, int first,
     }
 }
 
+// Consumer start: wait for the previous kernel on the stream (as in the
+// producer: it may still be writing `out`), then give empty (or invalid,
+// clamped to empty) sequences a zero output (decode: row s; append: its
+// query rows, when it has any).
+template <int D>
+__device__ __forceinline__ void zero_empty_outputs(const Params &p, int cw, int lane) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int Hq = p.n_q_heads;
+    for (int s = blockIdx.x; s < p.n_seqs; s += gridDim.x) {
+        if (p.lens[s] <= 0) {
+            const int r0 = p.cu_q != nullptr ? p.cu_q[s] : s;
+            const int nr = p.cu_q != nullptr ? p.cu_q[s + 1] - r0 : 1;
+            for (long long e = cw * 32 + lane; e < (long long)nr * Hq * D; e += NCW * 32) {
+                const size_t o = (size_t)r0 * Hq * D + e;
+                if (p.out_f32) static_cast<float *>(p.out)[o] = 0.0f;
+                else static_cast<__half *>(p.out)[o] = __float2half_rn(0.0f);
+            }
+        }
+    }
+}
+
+// Span schedule, when a consumer warp has no items left: count its cut parts
+// (record slots 0 / 1, bits of `pending`) in their pairs' arrivals.  One
+// fence releases the records (this warp's lanes wrote them before the
+// __syncwarp), then both increments are in flight together.  The part that
+// draws a pair's last count (n_parts * arrive of them) acquires and merges
+// the pair's records.
+template <int D, int G, int HG>
+__device__ __forceinline__ void count_pending(const Params &p, const PendPart (&pend)[2], int pending, int arrive,
+                                              int hl, int lane) {
+    __syncwarp();
+    unsigned got0 = 0, got1 = 0;
+    if (lane == 0) {
+        fence_acq_rel_gpu();
+        if (pending & 1)
+            got0 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pend[0].first * HG + hl,
+                                          (unsigned)(pend[0].n_parts * arrive - 1));
+        if (pending & 2)
+            got1 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pend[1].first * HG + hl,
+                                          (unsigned)(pend[1].n_parts * arrive - 1));
+    }
+    got0 = __shfl_sync(FULL, got0, 0);
+    got1 = __shfl_sync(FULL, got1, 0);
+    const PendPart pp0 = pend[0];
+    const PendPart pp1 = pend[1];
+    const bool last0 = (pending & 1) && got0 == (unsigned)(pp0.n_parts * arrive - 1);
+    const bool last1 = (pending & 2) && got1 == (unsigned)(pp1.n_parts * arrive - 1);
+    if (last0 || last1) {
+        if (lane == 0) fence_acq_rel_gpu();
+        __syncwarp();
+        if (last0)
+            merge_pair<D, G, HG>(p, kSpanPart, pp0.first, pp0.z_first, pp0.n_parts, pp0.qrow0, pp0.nq, pp0.h0 + hl,
+                                 hl, lane);
+        if (last1)
+            merge_pair<D, G, HG>(p, kSpanPart, pp1.first, pp1.z_first, pp1.n_parts, pp1.qrow0, pp1.nq, pp1.h0 + hl,
+                                 hl, lane);
+    }
+}
+
+// Span schedule: note a finished cut part (lane 0; written to the warp's
+// pend slot d.c).  Units a .. a + b - 1 of the pair are the cost unit, then
+// the tiles; its parts are spans owner(a) .. owner(a + b - 1), and the
+// first uses slot 1 when the pair starts inside it.
+__device__ __forceinline__ PendPart pending_part(const Params &p, const int *pre, const ItemDesc &d) {
+    const SpanMap map((long long)pre[p.n_seqs] * p.n_groups, gridDim.x);
+    const long long first = map.owner((long long)d.a + kPairCost);
+    PendPart pp;
+    pp.s = d.s;
+    pp.h0 = d.h0;
+    pp.first = (int)first;
+    pp.z_first = (long long)d.a <= map.start(first) ? 0 : 1;   // the span's first segment?
+    pp.n_parts = (int)(map.owner((long long)d.a + d.b - 1) - first + 1);
+    pp.qrow0 = d.qrow0;
+    pp.nq = d.nq;
+    return pp;
+}
+
 template <int D, int G, int HG>
 __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, int cw, int lane) {
     constexpr int NS = Shape<D, HG>::NS;
@@ -731,23 +866,8 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
     const int part = cw % WPH;        // which share of the head's rows, or of each tile's tokens
     const int row0 = RSPLIT ? part * R : 0;
     const int tok_base = RSPLIT ? 0 : part * TPT;
-    const int Hq = p.n_q_heads;
 
-    // (as in the producer: the previous kernel may still be writing `out`)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    // Empty (or invalid, clamped to empty) sequences get a zero output
-    // (decode: row s; append: its query rows, when it has any).
-    for (int s = blockIdx.x; s < p.n_seqs; s += gridDim.x) {
-        if (p.lens[s] <= 0) {
-            const int r0 = p.cu_q != nullptr ? p.cu_q[s] : s;
-            const int nr = p.cu_q != nullptr ? p.cu_q[s + 1] - r0 : 1;
-            for (long long e = cw * 32 + lane; e < (long long)nr * Hq * D; e += NCW * 32) {
-                const size_t o = (size_t)r0 * Hq * D + e;
-                if (p.out_f32) static_cast<float *>(p.out)[o] = 0.0f;
-                else static_cast<__half *>(p.out)[o] = __float2half_rn(0.0f);
-            }
-        }
-    }
+    zero_empty_outputs<D>(p, cw, lane);
 
     uint32_t st = 0;
     uint32_t cphase = 0;
@@ -758,44 +878,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
         if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
         const ItemDesc d = sm.desc[slot];
         if (d.s < 0) {
-            if (pending) {
-                // Count this warp's cut parts in their pairs' arrivals: one
-                // fence releases the records (this warp's lanes wrote them
-                // before the __syncwarp), then both increments are in flight
-                // together.  The part that draws a pair's last count acquires
-                // and merges the pair's records.
-                __syncwarp();
-                unsigned got0 = 0, got1 = 0;
-                if (lane == 0) {
-                    fence_acq_rel_gpu();
-                    if (pending & 1) {
-                        const PendPart &pp = sm.pend[cw][0];
-                        got0 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pp.first * HG + hl,
-                                                      (unsigned)(pp.n_parts * ARRIVE - 1));
-                    }
-                    if (pending & 2) {
-                        const PendPart &pp = sm.pend[cw][1];
-                        got1 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pp.first * HG + hl,
-                                                      (unsigned)(pp.n_parts * ARRIVE - 1));
-                    }
-                }
-                got0 = __shfl_sync(FULL, got0, 0);
-                got1 = __shfl_sync(FULL, got1, 0);
-                const PendPart pp0 = sm.pend[cw][0];
-                const PendPart pp1 = sm.pend[cw][1];
-                const bool last0 = (pending & 1) && got0 == (unsigned)(pp0.n_parts * ARRIVE - 1);
-                const bool last1 = (pending & 2) && got1 == (unsigned)(pp1.n_parts * ARRIVE - 1);
-                if (last0 || last1) {
-                    if (lane == 0) fence_acq_rel_gpu();
-                    __syncwarp();
-                    if (last0)
-                        merge_pair<D, G, HG>(p, kSpanPart, pp0.first, pp0.z_first, pp0.n_parts, pp0.qrow0, pp0.nq,
-                                             pp0.h0 + hl, hl, lane);
-                    if (last1)
-                        merge_pair<D, G, HG>(p, kSpanPart, pp1.first, pp1.z_first, pp1.n_parts, pp1.qrow0, pp1.nq,
-                                             pp1.h0 + hl, hl, lane);
-                }
-            }
+            if (pending) count_pending<D, G, HG>(p, sm.pend[cw], pending, ARRIVE, hl, lane);
             return;
         }
         const int h = d.h0 + hl;
@@ -1007,35 +1090,330 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 write_part<D, G, HG, R>(p, sm, d, hl, lane, row0, d.b == 0 && hl == 0 && part == 0, m, l, acc);
             } else {
                 // Span part: write the record and note the pair; it is
-                // counted when this CTA has no items left.  The pair's parts
-                // are spans owner(a) .. owner(a + b - 1); the first uses
-                // slot 1 when the pair starts inside it.
+                // counted when this CTA has no items left.
                 write_part<D, G, HG, R>(p, sm, d, hl, lane, row0, false, m, l, acc);
-                if (lane == 0) {
-                    // units a .. a + b - 1: the cost unit, then the tiles
-                    const SpanMap map((long long)sm.pre[p.n_seqs] * p.n_groups, gridDim.x);
-                    const long long first = map.owner((long long)d.a + kPairCost);
-                    PendPart pp;
-                    pp.s = d.s;
-                    pp.h0 = d.h0;
-                    pp.first = (int)first;
-                    pp.z_first = (long long)d.a <= map.start(first) ? 0 : 1;   // the span's first segment?
-                    pp.n_parts = (int)(map.owner((long long)d.a + d.b - 1) - first + 1);
-                    pp.qrow0 = d.qrow0;
-                    pp.nq = d.nq;
-                    sm.pend[cw][d.c] = pp;
-                }
+                if (lane == 0) sm.pend[cw][d.c] = pending_part(p, sm.pre, d);
                 pending |= 1 << d.c;
             }
         }
     }
 }
 
+// ------------------------------------------------------------ tensor-core consumers
+
+// Byte offset, in an MMA stage (one kv-head), of 16-byte chunk c (dims
+// 8c .. 8c + 7) of tile row t: per 64-dim half, TB rows of 128 bytes, chunk
+// c % 8 of row t stored at position (c % 8) ^ (t % 8) -- the layout a TMA
+// copy with 128-byte swizzling writes at a 1024-byte aligned stage.
+__device__ __forceinline__ uint32_t swz(int t, int c) {
+    return (uint32_t)((((c >> 3) * TB + t) << 7) + ((((c & 7) ^ (t & 7))) << 4));
+}
+
+// Two consecutive output values of one row.
+__device__ __forceinline__ void store2(const Params &p, size_t o, float x0, float x1) {
+    if (p.out_f32) *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + o) = make_float2(x0, x1);
+    else *reinterpret_cast<__half2 *>(static_cast<__half *>(p.out) + o) = __floats2half2_rn(x0, x1);
+}
+
+// Consumers for kv-heads with many rows (q-heads, or query tokens x
+// q-heads), HG kv-heads per item.  A head's rows (at most 16) form the M side
+// of warp-level tensor-core products, fp16 in, fp32 accumulate: scores
+// S = Q K^T over a 16-token tile (m16n8k16, two 8-token column blocks), then
+// O += P V with P the tile's weights rounded to fp16 (m16n8k16 per 8 dims).
+// The online softmax runs on the score fragments: lane (g, t) = (lane / 4,
+// lane % 4) holds rows g and g + 8, tokens 2t, 2t + 1 of each column block,
+// and the same rows of O at dims 8b + 2t, 8b + 2t + 1.  The weights' row sums
+// l are the sums of the rounded fp16 weights, so the normalised output is an
+// exact weighted mean of V under those weights.
+//
+// Each head has WPH = NCW / HG consumer warps; its tiles are dealt
+// round-robin (warp part p computes tiles j = p mod WPH, whole).  With
+// several warps per head their states meet in shared memory at the end and
+// the head's first warp carries the merged state on.
 template <int D, int G, int HG>
+__device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, true> &sm, int cw, int lane) {
+    constexpr int NS = Smem<D, G, HG, true>::NS;
+    constexpr int WPH = NCW / HG;   // consumer warps per head
+    constexpr int NKS = D / 16;     // k-steps of the score product
+    constexpr int NNB = D / 8;      // 8-dim column blocks of O
+    constexpr int CH = D / 8;       // 16-byte chunks of a row
+    static_assert(G <= 16, "the rows of a kv-head fill at most one m16 fragment");
+    static_assert(WPH * HG == NCW, "heads per item divide the consumer warps");
+    const int gq = lane >> 2;
+    const int tq = lane & 3;
+    const int hl = cw / WPH;        // head within the item
+    const int part = cw % WPH;      // which of the head's tiles this warp computes
+    const uint32_t hoff = (uint32_t)hl * (D / 64) * TB * 128;   // the head's bytes in a stage
+    const int Hq = p.n_q_heads;
+
+    zero_empty_outputs<D>(p, cw, lane);
+
+    uint32_t st = 0;
+    uint32_t cphase = 0;
+    const uint32_t cbar = smem_addr(&sm.cbar);
+    int pending = 0;   // span schedule: bit c = a cut part with record slot c awaits its count
+    for (int k = 0;; ++k) {
+        const int slot = k % NQ;
+        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
+        const ItemDesc d = sm.desc[slot];
+        if (d.s < 0) {
+            if (pending) count_pending<D, G, HG>(p, sm.pend[cw], pending, 1, hl, lane);
+            return;
+        }
+        const int h = d.h0 + hl;
+        const bool active = h < p.n_kv_heads;   // ragged last group: idle warps keep the protocol
+
+        // Fragment rows gq and gq + 8.  Row g: query token g / gh, q-head
+        // g % gh, sees tokens 0 .. lim; a row past the item's rows repeats
+        // row 0 (its results are dropped).
+        int lim[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int g = gq + 8 * r;
+            const int i = g / p.gh;
+            lim[r] = d.L - d.nq + ((g < G && i < d.nq) ? i : 0);
+        }
+        // q as A fragments, one ldmatrix.x4 per k-step: lanes 0-7 / 8-15 /
+        // 16-23 / 24-31 give rows 0-7 / 8-15 / 0-7 / 8-15 at dims +0 / +0 /
+        // +8 / +8.  Row g of head hl is at ((i * HG + hl) * gh + g % gh) * D.
+        uint32_t qa[NKS][4];
+        {
+            const int g = (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int gg = (g < G && g / p.gh < d.nq) ? g : 0;
+            const int i = gg / p.gh;
+            const uint32_t qrow = smem_addr(&sm.q[slot][((i * HG + hl) * p.gh + gg - i * p.gh) * D]) +
+                                  (uint32_t)(lane >> 4) * 16u;
+#pragma unroll
+            for (int ks = 0; ks < NKS; ++ks) ldmatrix_x4(qa[ks], qrow + ks * 32);
+        }
+        // Fused decode step: lanes 0 .. 2 CH - 1 keep one 16-byte chunk of
+        // the new token's K (lanes < CH) or V row of the head; the head's
+        // first warp writes the rows to the pool slot, and the warp that
+        // computes the item's last tile puts them in place of its row L - 1.
+        uint4 nrow = make_uint4(0u, 0u, 0u, 0u);
+        if (d.newrow >= 0 && active && lane < 2 * CH) {
+            nrow = *reinterpret_cast<const uint4 *>(&sm.knew[slot][lane / CH][hl * D + (lane % CH) * 8]);
+            if (part == 0 && d.newslot >= 0) {
+                const size_t dst = ((size_t)d.newslot * p.n_kv_heads + h) * D + (lane % CH) * 8;
+                *reinterpret_cast<uint4 *>((lane < CH ? p.k_pool : p.v_pool) + dst) = nrow;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(&sm.qempty[slot]));
+
+        float m[2] = {-INFINITY, -INFINITY};
+        float l[2] = {0.0f, 0.0f};
+        float o[NNB][4];
+#pragma unroll
+        for (int b = 0; b < NNB; ++b) o[b][0] = o[b][1] = o[b][2] = o[b][3] = 0.0f;
+
+        const int ntiles = (d.ntok + TB - 1) / TB;
+        for (int j = 0; j < ntiles; ++j, ++st) {
+            const int stage = st % NS;
+            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane)) return;
+            if (active && (j % WPH) == part) {
+                uint8_t *kt = reinterpret_cast<uint8_t *>(sm.k[stage]) + hoff;
+                uint8_t *vt = reinterpret_cast<uint8_t *>(sm.v[stage]) + hoff;
+                const uint32_t kb = smem_addr(kt);
+                const uint32_t vb = smem_addr(vt);
+                const int tile0 = d.tok0 + j * TB;
+                // tiles that reach a row's limit or the sequence's end
+                const bool masked = tile0 + TB > d.L - d.nq;
+                const int newr = (d.newrow >= 0 && j == ntiles - 1) ? d.newrow - tile0 : -1;
+                if (newr >= 0 || masked) {
+                    // patch the head's part of the stage: the new token's
+                    // rows, and zeros over V rows past the sequence's end
+                    // (they may hold anything; a zero weight times a
+                    // non-finite value would not vanish)
+                    if (newr >= 0 && lane < 2 * CH)
+                        *reinterpret_cast<uint4 *>((lane < CH ? kt : vt) + swz(newr, lane % CH)) = nrow;
+                    if (masked) {
+                        const int nvalid = d.L - tile0;
+                        for (int e = lane; e < TB * CH; e += 32) {
+                            const int t = e / CH;
+                            if (t >= nvalid) *reinterpret_cast<uint4 *>(vt + swz(t, e % CH)) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    }
+                    // the stage is refilled by TMA (async proxy) later
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                }
+                // S = Q K^T: K rows are the B fragments' columns (tokens);
+                // one ldmatrix.x4 gives two k-steps of one column block
+                float sc[2][4];
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) {
+                    sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
+#pragma unroll
+                    for (int kp = 0; kp < NKS / 2; ++kp) {
+                        uint32_t b[4];
+                        ldmatrix_x4(b, kb + swz(nb * 8 + (lane & 7), kp * 4 + (lane >> 3)));
+                        mma_f16_16816(sc[nb], qa[2 * kp], b[0], b[1]);
+                        mma_f16_16816(sc[nb], qa[2 * kp + 1], b[2], b[3]);
+                    }
+                }
+                // scaled scores (log2 domain) with the limits applied
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        sc[nb][e] *= p.scale_log2;
+                        if (masked && tile0 + nb * 8 + 2 * tq + (e & 1) > lim[e >> 1]) sc[nb][e] = -INFINITY;
+                    }
+                }
+                // the rows' maxima over the tile (the 4 lanes of a row
+                // group); the reference m is raised only when the tile passes
+                // it by more than 2^8
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    float mt = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
+                    mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
+                    mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
+                    if (mt > m[r] + kRescaleLog2) {
+                        const float f = exp2f(m[r] - mt);   // m = -inf gives 0
+                        l[r] *= f;
+#pragma unroll
+                        for (int b = 0; b < NNB; ++b) {
+                            o[b][2 * r] *= f;
+                            o[b][2 * r + 1] *= f;
+                        }
+                        m[r] = mt;
+                    }
+                }
+                // weights as the A fragment of P V: register 2 nb + r holds
+                // row g + 8 r, tokens 8 nb + 2t, 8 nb + 2t + 1
+                uint32_t pa[4];
+#pragma unroll
+                for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        const float z0 = sc[nb][2 * r], z1 = sc[nb][2 * r + 1];
+                        const float p0 = z0 == -INFINITY ? 0.0f : exp2f(z0 - m[r]);
+                        const float p1 = z1 == -INFINITY ? 0.0f : exp2f(z1 - m[r]);
+                        const __half2 w = __floats2half2_rn(p0, p1);
+                        const float2 wf = __half22float2(w);
+                        l[r] += wf.x + wf.y;
+                        pa[2 * nb + r] = *reinterpret_cast<const uint32_t *>(&w);
+                    }
+                }
+                // O += P V: V rows (tokens) are the B fragments' k; one
+                // ldmatrix.x4.trans gives two 8-dim column blocks
+#pragma unroll
+                for (int np = 0; np < NNB / 2; ++np) {
+                    uint32_t b[4];
+                    ldmatrix_x4_trans(b, vb + swz((lane & 7) + ((lane >> 3) & 1) * 8, np * 2 + (lane >> 4)));
+                    mma_f16_16816(o[2 * np], pa, b[0], b[1]);
+                    mma_f16_16816(o[2 * np + 1], pa, b[2], b[3]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_addr(&sm.empty[stage]));
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            l[r] += __shfl_xor_sync(FULL, l[r], 1);
+            l[r] += __shfl_xor_sync(FULL, l[r], 2);
+        }
+
+        if (WPH > 1 && ntiles > 1) {
+            // The head's warps' states meet in shared memory (rows < G); its
+            // first warp merges them with the log-sum-exp rule.
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int g = gq + 8 * r;
+                if (g < G) {
+                    float *rw = sm.red[cw][g];
+#pragma unroll
+                    for (int b = 0; b < NNB; ++b)
+                        *reinterpret_cast<float2 *>(rw + b * 8 + 2 * tq) = make_float2(o[b][2 * r], o[b][2 * r + 1]);
+                    if (tq == 0) {
+                        rw[D] = m[r];
+                        rw[D + 1] = l[r];
+                    }
+                }
+            }
+            if (!warps_sync(cbar, cphase, p.status, lane)) return;
+            if (part == 0) {
+                const int w0 = hl * WPH;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int g = gq + 8 * r;
+                    if (g >= G) continue;
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int w = 0; w < WPH; ++w) mx = fmaxf(mx, sm.red[w0 + w][g][D]);
+                    float ls = 0.0f;
+                    float a[NNB][2];
+#pragma unroll
+                    for (int b = 0; b < NNB; ++b) a[b][0] = a[b][1] = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < WPH; ++w) {
+                        const float mw = sm.red[w0 + w][g][D];
+                        const float f = mw == -INFINITY ? 0.0f : exp2f(mw - mx);
+                        ls = fmaf(sm.red[w0 + w][g][D + 1], f, ls);
+#pragma unroll
+                        for (int b = 0; b < NNB; ++b) {
+                            const float2 v = *reinterpret_cast<const float2 *>(&sm.red[w0 + w][g][b * 8 + 2 * tq]);
+                            a[b][0] = fmaf(v.x, f, a[b][0]);
+                            a[b][1] = fmaf(v.y, f, a[b][1]);
+                        }
+                    }
+                    m[r] = mx;
+                    l[r] = ls;
+#pragma unroll
+                    for (int b = 0; b < NNB; ++b) {
+                        o[b][2 * r] = a[b][0];
+                        o[b][2 * r + 1] = a[b][1];
+                    }
+                }
+            }
+            if (!warps_sync(cbar, cphase, p.status, lane)) return;   // red[] is reused next item
+        }
+        if (part != 0 || !active) continue;
+        if (d.kind == kWhole) {
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int g = gq + 8 * r;
+                const int i = g / p.gh;
+                if (g >= G || i >= d.nq) continue;
+                const float inv = 1.0f / l[r];
+                const size_t ob = ((size_t)(d.qrow0 + i) * Hq + (size_t)h * p.gh + g - i * p.gh) * D + 2 * tq;
+#pragma unroll
+                for (int b = 0; b < NNB; ++b) store2(p, ob + b * 8, o[b][2 * r] * inv, o[b][2 * r + 1] * inv);
+            }
+        } else {
+            // Span part: write the record ((span * 2 + slot) * HG + head)
+            // and note the pair; it is counted when this CTA has no items left.
+            float *part_rec = p.partials + (((size_t)d.span * 2 + d.c) * HG + hl) * (size_t)(G * (D + 2));
+#pragma unroll
+            for (int r = 0; r < 2; ++r) {
+                const int g = gq + 8 * r;
+                if (g >= G) continue;
+                float *rw = part_rec + g * (D + 2);
+#pragma unroll
+                for (int b = 0; b < NNB; ++b)
+                    *reinterpret_cast<float2 *>(rw + b * 8 + 2 * tq) = make_float2(o[b][2 * r], o[b][2 * r + 1]);
+                if (tq == 0) {
+                    rw[D] = m[r];
+                    rw[D + 1] = l[r];
+                }
+            }
+            if (lane == 0) sm.pend[cw][d.c] = pending_part(p, sm.pre, d);
+            pending |= 1 << d.c;
+        }
+    }
+}
+
+template <int D, int G, int HG, bool MMA = false>
 __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p) {
-    constexpr int NS = Shape<D, HG>::NS;
+    using SM = Smem<D, G, HG, MMA>;
+    constexpr int NS = SM::NS;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    Smem<D, G, HG> &sm = *reinterpret_cast<Smem<D, G, HG> *>(smem_raw);
+    uint8_t *base = smem_raw;
+    // MMA: the swizzled stages need a 1024-byte aligned struct (the launch
+    // adds 1 KB of slack for this)
+    if constexpr (MMA) base += (1024u - (smem_addr(smem_raw) & 1023u)) & 1023u;
+    SM &sm = *reinterpret_cast<SM *>(base);
     const int warp = threadIdx.x / 32;
     const int lane = threadIdx.x % 32;
     // The merge grid that follows may start launching now; it waits for
@@ -1074,7 +1452,7 @@ __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const C
                 atomicOr(p.status, PF_DEV_BAD_LENGTH);
                 L = L < 0 ? 0 : maxctx;
             }
-            L = append_length(p, s, L, G);
+            L = append_length(p, s, L);
             sm.rem[s] = (uint8_t)(L - (L - 1) / TB * TB);   // unused when L = 0
             sm.pre[s + 1] = L > 0 ? (L + TB - 1) / TB + kPairCost : 0;
         }
@@ -1101,7 +1479,8 @@ __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const C
         if (threadIdx.x == 0) sm.pre[0] = 0;
     }
     __syncthreads();
-    if (warp == 0) producer<D, G, HG>(&tmk, &tmv, p, sm, lane);
+    if (warp == 0) producer<D, G, HG, MMA>(&tmk, &tmv, p, sm, lane);
+    else if constexpr (MMA) consumers_mma<D, G, HG>(p, sm, warp - 1, lane);
     else consumers<D, G, HG>(p, sm, warp - 1, lane);
 }
 
@@ -1131,6 +1510,22 @@ __global__ void __maxnreg__(128) paged_decode_kernel_r128(const __grid_constant_
     decode_attention<D, G, HG>(tmk, tmv, p);
 }
 
+// Tensor-core consumers, HG kv-heads per item (span schedule, block size
+// >= TB).  At head_dim 64 the state fits 128 registers (3 CTAs per SM); at
+// 128, 2 CTAs put up to 3 warps on a sub-partition: 168 registers.
+template <int D, int G, int HG>
+__global__ void __maxnreg__(168) paged_decode_kernel_mma(const __grid_constant__ CUtensorMap tmk,
+                                                         const __grid_constant__ CUtensorMap tmv, const Params p) {
+    decode_attention<D, G, HG, true>(tmk, tmv, p);
+}
+
+template <int D, int G, int HG>
+__global__ void __maxnreg__(128) paged_decode_kernel_mma_r128(const __grid_constant__ CUtensorMap tmk,
+                                                              const __grid_constant__ CUtensorMap tmv,
+                                                              const Params p) {
+    decode_attention<D, G, HG, true>(tmk, tmv, p);
+}
+
 // Chunk schedule: merge the records of every job of this launch's epoch, one
 // warp per (job slot, head).  A head costs about two dependent memory round
 // trips (the job, then its records).
@@ -1148,7 +1543,7 @@ __global__ void __launch_bounds__(128, 1) merge_kernel(const Params p, int n_job
         int qrow0 = jb.s, nq = 1;
         if (p.cu_q != nullptr) {
             qrow0 = p.cu_q[jb.s];
-            nq = max(1, min(p.cu_q[jb.s + 1] - qrow0, G / p.gh));
+            nq = max(1, min(p.cu_q[jb.s + 1] - qrow0, p.rows / p.gh));
         }
         merge_pair<D, G, HG>(p, jb.kind, jb.first, jb.z_first, jb.n_parts, qrow0, nq, jb.h0 + hl, hl, lane);
     }
@@ -1161,11 +1556,41 @@ struct KernelInfo {
     KernelFn fn;
     size_t smem;
     MergeFn merge;
+    int rows;   // rows per kv-head of the instance (its G): the size of a record's rows
 };
 
-// Defined in attention_d64.cu / attention_d128.cu.
+// Defined in attention_d64.cu / attention_d128.cu / attention_mma.cu (the
+// tensor-core instances: span schedule only, no merge kernel; smem includes
+// 1 KB of alignment slack).
 KernelInfo kernel_d64(int g, int hg);
 KernelInfo kernel_d128(int g, int hg);
+// Tensor-core instances: rows per kv-head rounded up to 4, 8 (the "_s"
+// files) or 12, 16; hg 1, 2 or 4 (not 4 at head_dim 128 above 8 rows).
+KernelInfo kernel_mma_d64_s(int g, int hg);
+KernelInfo kernel_mma_d64_l(int g, int hg);
+KernelInfo kernel_mma_d128_s(int g, int hg);
+KernelInfo kernel_mma_d128_l(int g, int hg);
+
+template <int D, int G, int HG>
+KernelInfo mma_info() {
+    constexpr size_t smem = sizeof(Smem<D, G, HG, true>) + 1024;
+    // with the 1 KB each CTA reserves: 3 CTAs per SM (228 KB) at head_dim 64, 2 at 128
+    static_assert(smem + 1024 <= (D == 64 ? 228 * 1024 / 3 : 228 * 1024 / 2), "shared memory per CTA");
+    if constexpr (D == 64) return {paged_decode_kernel_mma_r128<D, G, HG>, smem, nullptr, G};
+    else return {paged_decode_kernel_mma<D, G, HG>, smem, nullptr, G};
+}
+
+template <int D, int G>
+KernelInfo mma_by_heads(int hg) {
+    switch (hg) {
+        case 1: return mma_info<D, G, 1>();
+        case 2: return mma_info<D, G, 2>();
+        case 4:
+            if constexpr (D == 64 || G <= 8) return mma_info<D, G, 4>();
+            else return {nullptr, 0, nullptr, 0};
+        default: return {nullptr, 0, nullptr, 0};
+    }
+}
 
 }  // namespace attn
 }  // namespace pkv

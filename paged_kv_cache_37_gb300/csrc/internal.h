@@ -40,10 +40,11 @@ struct pf_pool {
     // TMA descriptors over K and V viewed as [rows][n_kv_heads][head_dim]
     // with rows = n_layers * n_blocks * block_size, encoded lazily per device.
     std::mutex mu;
-    // [device][hg index: 0, 1, 2 for 1, 2, 4 kv-heads per box]
-    bool tmap_ready[pkv::kMaxDevices][3];
-    CUtensorMap tmap_k[pkv::kMaxDevices][3];
-    CUtensorMap tmap_v[pkv::kMaxDevices][3];
+    // [device][0, 1, 2: boxes of 1, 2, 4 kv-heads; 3: the tensor-core
+    // layout (one kv-head, swizzled 64-element halves)]
+    bool tmap_ready[pkv::kMaxDevices][4];
+    CUtensorMap tmap_k[pkv::kMaxDevices][4];
+    CUtensorMap tmap_v[pkv::kMaxDevices][4];
 };
 
 namespace pkv {
@@ -55,8 +56,9 @@ int *device_status_ptr();
 // entry point has used it (synchronous on the stream).
 int noalloc_scratch_reset(cudaStream_t stream);
 
-// TMA descriptors of the pool for boxes of hg (1, 2 or 4) kv-heads on
-// `device`, encoded on first use; *index receives their slot.
+// TMA descriptors of the pool for boxes of hg (1, 2 or 4) kv-heads, or (hg
+// = 0) the tensor-core layout, on `device`, encoded on first use; *index
+// receives their slot.
 int encode_pool_tmaps(pf_pool *pool, int device, int hg, int *index);
 
 struct WriteArgs {

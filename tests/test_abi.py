@@ -78,11 +78,15 @@ def test_device_calls_reject_bad_arguments_before_launch(pkv):
     assert lib.pf_write_kv(pool, 0, None, None, None, 0, 0, None, None, 0, None) == pkv.PF_OK
     assert lib.pf_gather_kv(pool, 0, ok, 7, ok, ok, 4, None, ok, None) == pkv.PF_ERR_INVALID
     assert lib.pf_gather_kv(pool, 0, ok, 7, ok, ok, 0, None, None, None) == pkv.PF_OK
-    # attention: q-heads not a multiple of kv-heads, group > 8, bad dtype, bad scale, small workspace
+    # attention: q-heads not a multiple of kv-heads, group > 16 (> 8 unless balanced), bad dtype, bad scale, small workspace
     args = lambda hq=12, dt=1, scale=0.125, ws=1 << 20, split=0: (
         pool, 0, ok, ok, 7, ok, 4, hq, ctypes.c_float(scale), ok, dt, split, ok, ws, None)
     assert lib.pf_paged_decode_attention(*args(hq=13)) == pkv.PF_ERR_INVALID
-    assert lib.pf_paged_decode_attention(*args(hq=12 * 9)) == pkv.PF_ERR_UNSUPPORTED
+    assert lib.pf_paged_decode_attention(*args(hq=12 * 17)) == pkv.PF_ERR_UNSUPPORTED
+    assert lib.pf_paged_decode_attention(*args(hq=12 * 9, split=-1)) == pkv.PF_ERR_UNSUPPORTED
+    assert lib.pf_paged_decode_attention(*args(hq=12 * 9, split=64)) == pkv.PF_ERR_UNSUPPORTED
+    assert lib.pf_decode_workspace_bytes(pool, 4, 12 * 16, 7, 0) > 0    # 16 rows: balanced schedule only
+    assert lib.pf_decode_workspace_bytes(pool, 4, 12 * 16, 7, -1) == 0
     assert lib.pf_paged_decode_attention(*args(dt=3)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_decode_attention(*args(scale=0.0)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_decode_attention(*args(scale=float("nan"))) == pkv.PF_ERR_INVALID

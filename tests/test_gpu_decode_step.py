@@ -76,6 +76,20 @@ def test_step_edge_lengths_fp32(pkv, cuda_dev, oracle_mod, split):
     assert np.array_equal(fused.view(np.uint32), unfused.view(np.uint32))
 
 
+@pytest.mark.parametrize("hq,hkv,d,b", [(32, 4, 128, 16), (16, 1, 64, 64), (12, 1, 128, 16), (8, 2, 64, 16)])
+def test_step_many_rows(pkv, cuda_dev, oracle_mod, hq, hkv, d, b):
+    """4 to 16 q-heads per kv-head (the tensor-core consumers), the new row
+    substituted in the tile, ragged tails and empty sequences, fp32 out."""
+    lens = np.array([0] + list(range(1, 40)) + list(si.uniform_lengths(20, 40, 900, seed=14)), dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, hq, hkv, d, b)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    fused, unfused, ref = _run_both(pkv, cuda_dev, oracle_mod, c, scale, out_f32=True)
+    assert np.all(fused[0] == 0)
+    assert_close_to_oracle(fused, ref, what=f"step {hq}/{hkv}x{d} B={b}")
+    assert np.array_equal(fused.view(np.uint32), unfused.view(np.uint32))
+    assert pkv.pf_device_status(reset=True) == 0
+
+
 def test_step_13b_like(pkv, cuda_dev, oracle_mod):
     w = si.WORKLOADS["13b"]
     lens = np.array([2048, 2000, 17, 1], dtype=np.int32)
