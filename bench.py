@@ -621,7 +621,8 @@ def run_ours(args, dist):
         "append_attention": {"new_tokens_per_seq": n_app, "ms": round(app_ms, 5), "bytes": app_bytes,
                              "gbs": round(app_bytes / (app_ms / 1e3) / 1e9, 1),
                              "frac_of_measured_copy": round(app_bytes / (app_ms / 1e3) / 1e9 / peak, 4),
-                             "kernel": "paged_decode_kernel (8 rows per kv-head, workspace path)",
+                             "kernel": "paged_decode_kernel_mma_r128<64,8,4> (8 rows per kv-head on tensor cores, "
+                                       "workspace path)",
                              "without_workspace_ms": round(app2_ms, 5),
                              "without_workspace_gbs": round(app_bytes / (app2_ms / 1e3) / 1e9, 1)},
         "prompt_prefill": {"prompts": Sp, "tokens": Lp, "ms": round(pr_ms, 4), "flops": pr_flops,
@@ -630,7 +631,8 @@ def run_ours(args, dist):
                            "frac": round(pr_flops / (pr_ms / 1e3) / 1e12 / fp32_peak, 4),
                            "peak_note": "SMs x 128 fp32 lanes x 2 flop x max SM clock (CUDA cores, no tensor cores)"},
         "gqa_attention": {"workload": "256 sequences of U[32,4096] tokens, 14 q-heads / 2 kv-heads x 64, "
-                                      "block 16, shuffled frames", "ms": round(gqa_ms, 5), "bytes": gqa_bytes,
+                                      "block 16, shuffled frames", "kernel": "paged_decode_kernel_mma_r128<64,8,2> "
+                                      "(7 rows per kv-head on tensor cores)", "ms": round(gqa_ms, 5), "bytes": gqa_bytes,
                           "gbs": round(gqa_bytes / (gqa_ms / 1e3) / 1e9, 1),
                           "frac_of_measured_copy": round(gqa_bytes / (gqa_ms / 1e3) / 1e9 / peak, 4)},
         "gather": {"gbs": round(g_bytes / (gather_ms / 1e3) / 1e9, 1), "ms": round(gather_ms, 5),

@@ -306,8 +306,9 @@ PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
  * PF_DEV_BAD_BLOCK_ID.
  * Two kernels: with a workspace (of pf_prefill_workspace_bytes bytes,
  * initialised once with pf_decode_workspace_init, not shared by overlapping
- * calls) and max_new_tokens x (n_q_heads / Hkv) <= 8, the decode kernel
- * serves the new tokens as extra rows of each kv-head -- balanced spans over
+ * calls) and max_new_tokens x (n_q_heads / Hkv) <= 8 (16 on pages of at
+ * least 16 tokens), the decode kernel serves the new tokens as extra rows of
+ * each kv-head -- balanced spans over
  * the contexts, every K/V byte read once per kv-head (a chunked append);
  * otherwise (workspace null, or longer appends and prompts) a kernel that
  * needs no workspace walks each (chunk of new tokens, kv-head) over its
@@ -323,8 +324,9 @@ PF_API int pf_paged_prefill_attention(const pf_pool *pool, int layer,
                                       void *workspace, size_t ws_bytes,
                                       void *stream);
 /* Workspace bytes of pf_paged_prefill_attention's decode-kernel path for
- * these sizes, or 0 when that path does not apply (more than 8 rows per
- * kv-head; the call then needs no workspace) or on bad arguments. */
+ * these sizes, or 0 when that path does not apply (more than 16 rows per
+ * kv-head, or 8 on pages of fewer than 16 tokens; the call then needs no
+ * workspace) or on bad arguments. */
 PF_API size_t pf_prefill_workspace_bytes(const pf_pool *pool, int n_seqs,
                                          int n_q_heads, int max_blocks_per_seq,
                                          int max_new_tokens);

@@ -302,10 +302,14 @@ int pf_decode_step(const pf_pool *pool, int layer, const void *q, const void *k_
 
 // Rows per kv-head when an append takes the decode kernel (its query tokens
 // x its q-heads), or 0 when they do not fit (the standalone kernel then).
+// Rows per kv-head of an append on the decode kernel (query tokens x
+// q-heads): up to 16 on pages of at least 16 tokens (the tensor-core
+// consumers take 9 and more), up to 8 otherwise; 0 = too many.
 static int append_rows(const pf_pool *pool, int n_q_heads, int max_new_tokens) {
     if (n_q_heads <= 0 || n_q_heads % pool->n_kv_heads) return 0;
     const long long rows = (long long)max_new_tokens * (n_q_heads / pool->n_kv_heads);
-    return rows >= 1 && rows <= 8 ? (int)rows : 0;
+    const int cap = pool->block_size >= 16 ? 16 : 8;
+    return rows >= 1 && rows <= cap ? (int)rows : 0;
 }
 
 size_t pf_prefill_workspace_bytes(const pf_pool *pool, int n_seqs, int n_q_heads, int max_blocks_per_seq,
@@ -318,7 +322,9 @@ size_t pf_prefill_workspace_bytes(const pf_pool *pool, int n_seqs, int n_q_heads
     const int rows = append_rows(pool, n_q_heads, max_new_tokens);
     if (rows == 0) return 0;   // the call takes the kernel that needs no workspace
     pkv::AttnPlan plan;
-    if (pkv::attention_plan(pool, n_seqs, rows * pool->n_kv_heads, max_blocks_per_seq, 0, true, &plan) != PF_OK)
+    // sized like pf_decode_workspace_bytes: by the resident grid, or by a
+    // bound on it when no device can be queried
+    if (pkv::attention_plan(pool, n_seqs, rows * pool->n_kv_heads, max_blocks_per_seq, 0, false, &plan) != PF_OK)
         return 0;
     return plan.counter_bytes + plan.partial_bytes;
 }

@@ -123,7 +123,8 @@ def test_device_calls_reject_bad_arguments_before_launch(pkv):
     assert lib.pf_paged_prefill_attention(*pre(n=-1)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_prefill_attention(*pre(dt=7)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_prefill_attention(*pre(mx=0)) == pkv.PF_OK
-    assert lib.pf_prefill_workspace_bytes(pool, 4, 12, 7, 9) == 0        # 9 rows per kv-head: no workspace path
+    assert lib.pf_prefill_workspace_bytes(pool, 4, 12, 7, 17) == 0       # 17 rows per kv-head: no workspace path
+    assert lib.pf_prefill_workspace_bytes(pool, 4, 12, 7, 16) > 0        # 16 rows on 16-token pages
     assert lib.pf_prefill_workspace_bytes(pool, 4, 12, 0, 2) == 0        # bad table width
     lib.pf_pool_destroy(pool)
 

@@ -90,7 +90,8 @@ def test_too_many_new_tokens_is_flagged(pkv, cuda_dev):
 
 
 def _run_ws(pkv, cuda_dev, c, n_new, scale, seed=500):
-    """The decode-kernel path: a workspace, at most 8 rows per kv-head."""
+    """The decode-kernel path: a workspace, at most 16 rows per kv-head (8 on
+    pages of fewer than 16 tokens)."""
     import torch
     cu = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
     mx = int(max(n_new.max(), 1))
@@ -105,7 +106,9 @@ def _run_ws(pkv, cuda_dev, c, n_new, scale, seed=500):
 
 
 @pytest.mark.parametrize("hq,hkv,d,b,mx", [(12, 12, 64, 16, 8), (14, 2, 64, 1, 1), (8, 4, 128, 64, 4),
-                                           (40, 40, 128, 16, 8), (16, 2, 64, 256, 1), (6, 3, 64, 16, 4)])
+                                           (40, 40, 128, 16, 8), (16, 2, 64, 256, 1), (6, 3, 64, 16, 4),
+                                           (12, 12, 64, 16, 16), (8, 4, 128, 64, 8), (4, 1, 64, 16, 4),
+                                           (4, 4, 64, 1, 8)])
 def test_short_append_on_the_decode_kernel(pkv, cuda_dev, oracle_mod, hq, hkv, d, b, mx):
     lens = si.uniform_lengths(30, 1, 1500, seed=26)
     rng = np.random.default_rng(7)
