@@ -16,7 +16,11 @@ the same kernels on ordered frames, the gather leg, the roofline of the
 attention kernel (CUDA events around every attention launch of the timed
 region), an end-to-end number through the public API with host buffers, the
 oracle timed on the host cores as a CPU baseline, SM clocks sampled during the
-timed work, and the number of kernel launches timed.
+timed work, and the number of kernel launches timed.  Side legs, timed after
+the main one: block copies and swaps, appends and prompts, grouped heads
+(14/2 x 64) over pages of 1, 16, 64 and 256 tokens, the 13B-like shape (40 x
+128 at 2048 tokens, batch 1..64, balanced vs no split) and a GPT-2-shaped
+12-layer, 50-step decode loop (eager and replayed from a CUDA graph).
 
 --impl reference times the fp64 CPU oracle on the same workload (the
 reference arm of this project).  --gpus N under torchrun runs N independent
@@ -138,6 +142,17 @@ def read_peaks():
         return float(d["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def read_tensor_peak():
+    """Dense fp16 tensor TFLOP/s: the measured bf16 burst figure (fp16 and bf16
+    have the same nominal dense rate), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
 
 
 def profile_traffic():
@@ -513,9 +528,117 @@ def run_ours(args, dist):
     gqa_ms = time_calls(lambda i: check(lib.pf_paged_decode_attention(*g_args[i % 2])), Kg)
     gqa_bytes = attention_bytes(g_lens, gHq, gHkv, gD, gB)
     del g_reps
+    # the same token counts stored in pages of 1, 64 and 256 tokens
+    gqa_sweep = [{"block_size": gB, "ms": round(gqa_ms, 5), "gbs": round(gqa_bytes / (gqa_ms / 1e3) / 1e9, 1)}]
+    for bs in (1, 64, 256):
+        sN = int(sum(-(-int(L_) // bs) for L_ in g_lens)) + 64
+        s_maxb = -(-int(g_lens.max()) // bs)
+        s_bt = to(si.block_tables(g_lens, bs, sN, si.SEED_SHUFFLE, max_blocks=s_maxb))
+        s_reps = []
+        for r in range(2):
+            sk = torch.empty((1, sN, bs, gHkv, gD), dtype=torch.float16, device=device).normal_()
+            sv = torch.empty_like(sk).normal_()
+            spool = pkv.pf_pool_create(sk, sv)
+            s_reps.append((sk, sv, spool, pkv.make_workspace(spool, wg["n_seqs"], gHq, s_maxb),
+                           torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device)))
+        gq0 = torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device).normal_()
+        s_args = [(sr[2].handle, 0, P(gq0), P(s_bt), s_maxb, P(g_lens_d), wg["n_seqs"], gHq,
+                   ctypes.c_float(wg["scale"]), P(sr[4]), pkv.PF_F16, 0, P(sr[3]), sr[3].numel(), sp) for sr in s_reps]
+        s_ms = time_calls(lambda i: check(lib.pf_paged_decode_attention(*s_args[i % 2])), max(10, Kg // 4))
+        s_bytes = attention_bytes(g_lens, gHq, gHkv, gD, bs)
+        gqa_sweep.append({"block_size": bs, "ms": round(s_ms, 5), "gbs": round(s_bytes / (s_ms / 1e3) / 1e9, 1)})
+        del s_reps, gq0
+
+    # 13B-like: 40 heads x 128, every sequence at 2048 tokens, batch 1 .. 64,
+    # the balanced schedule (split_tokens 0) against no split (-1).  One pool
+    # of 64 x 128 pages; a batch of S rotates over 64 / S disjoint table sets,
+    # so no call finds its pages in L2.
+    w13 = si.WORKLOADS["13b"]
+    c13, H13, D13, B13 = w13["context_len"], w13["n_q_heads"], w13["head_dim"], w13["block_size"]
+    pages13 = c13 // B13
+    N13 = 64 * pages13
+    k13 = torch.empty((1, N13, B13, H13, D13), dtype=torch.float16, device=device).normal_()
+    v13 = torch.empty_like(k13).normal_()
+    pool13 = pkv.pf_pool_create(k13, v13)
+    bt13 = si.block_tables(np.full(64, c13, dtype=np.int32), B13, N13, si.SEED_SHUFFLE, max_blocks=pages13)
+    split13 = []
+    for S13 in w13["batches"]:
+        sets = 64 // S13
+        tabs = [to(np.ascontiguousarray(bt13[j * S13:(j + 1) * S13])) for j in range(sets)]
+        l13 = to(np.full(S13, c13, dtype=np.int32))
+        q13 = torch.empty((S13, H13, D13), dtype=torch.float16, device=device).normal_()
+        o13 = torch.empty_like(q13)
+        row = {"batch": S13}
+        b13 = attention_bytes(np.full(S13, c13), H13, H13, D13, B13)
+        for name_, spl in (("balanced", 0), ("no_split", -1)):
+            ws13 = pkv.make_workspace(pool13, S13, H13, pages13, spl)
+            a13 = [(pool13.handle, 0, P(q13), P(t_), pages13, P(l13), S13, H13, ctypes.c_float(w13["scale"]),
+                    P(o13), pkv.PF_F16, spl, P(ws13), ws13.numel(), sp) for t_ in tabs]
+            ms13 = time_calls(lambda i: check(lib.pf_paged_decode_attention(*a13[i % sets])), 20)
+            row[name_ + "_us"] = round(ms13 * 1e3, 2)
+            row[name_ + "_gbs"] = round(b13 / (ms13 / 1e3) / 1e9, 1)
+        split13.append(row)
+    del k13, v13, pool13
+
+    # GPT-2-shaped decode loop: 12 layers x 12 heads x 64, 32 sequences with
+    # prompts of U[16, 64] tokens, 50 decode steps of one fused call per
+    # layer (launch-bound: ~9 MB per layer call).  Pages for the final
+    # lengths are allocated up front; step i attends over prompt + i + 1.
+    w2 = si.WORKLOADS["gpt2"]
+    S2, L2n, H2, D2, B2 = w2["n_seqs"], w2["n_layers"], w2["n_q_heads"], w2["head_dim"], w2["block_size"]
+    steps2 = w2["decode_steps"]
+    pr2 = si.uniform_lengths(S2, w2["prompt_lo"], w2["prompt_hi"])
+    N2 = S2 * w2["tokens_per_seq"] // B2
+    maxb2 = w2["tokens_per_seq"] // B2
+    bt2 = to(si.block_tables(pr2 + steps2, B2, N2, si.SEED_SHUFFLE, max_blocks=maxb2))
+    lens2 = to(np.stack([pr2 + i + 1 for i in range(steps2)]).astype(np.int32))
+    k2 = torch.empty((L2n, N2, B2, H2, D2), dtype=torch.float16, device=device).normal_()
+    v2 = torch.empty_like(k2).normal_()
+    pool2 = pkv.pf_pool_create(k2, v2)
+    q2 = torch.empty((L2n, S2, H2, D2), dtype=torch.float16, device=device).normal_()
+    kn2 = torch.empty((L2n, S2, H2, D2), dtype=torch.float16, device=device).normal_()
+    o2 = torch.empty_like(q2)
+    ws2 = pkv.make_workspace(pool2, S2, H2, maxb2, 0)
+    args2 = [[(pool2.handle, l_, P(q2[l_]), P(kn2[l_]), P(kn2[l_]), P(bt2), maxb2, P(lens2[i]), S2, H2,
+               ctypes.c_float(w2["scale"]), P(o2[l_]), pkv.PF_F16, 0, P(ws2), ws2.numel(),
+               pkv.PF_STEP_OVERLAP_PREVIOUS, sp) for l_ in range(L2n)] for i in range(steps2)]
+
+    def decode_loop(_):
+        for i in range(steps2):
+            for l_ in range(L2n):
+                check(lib.pf_decode_step(*args2[i][l_]))
+
+    loop_ms = time_calls(decode_loop, 5)
+    bytes2 = sum(attention_bytes(pr2 + i + 1, H2, H2, D2, B2) + write_bytes(S2, H2, D2) for i in range(steps2)) * L2n
+    gpt2 = {"workload": "12 layers x 12 heads x 64, 32 sequences, prompts U[16,64], 50 decode steps, block 16, "
+                        "pool of 512 tokens per sequence, shuffled frames",
+            "ms_per_decode_step": round(loop_ms / steps2, 5),
+            "us_per_layer_call": round(loop_ms / steps2 / L2n * 1e3, 2),
+            "tokens_per_s_per_layer": round(S2 / (loop_ms / steps2 / L2n / 1e3), 1),
+            "gbs": round(bytes2 / (loop_ms / 1e3) / 1e9, 1)}
+    # the same 600 calls replayed from a CUDA graph (launch cost removed)
+    try:
+        gstream = torch.cuda.Stream(device)
+        graph = torch.cuda.CUDAGraph()
+        gsp = ctypes.c_void_p(gstream.cuda_stream)
+        gargs = [[a_[:-1] + (gsp,) for a_ in row_] for row_ in args2]
+        with torch.cuda.stream(gstream):
+            decode_loop(0)   # warm on the capture stream
+        torch.cuda.synchronize(device)
+        with torch.cuda.graph(graph, stream=gstream):
+            for i in range(steps2):
+                for l_ in range(L2n):
+                    check(lib.pf_decode_step(*gargs[i][l_]))
+        graph_ms = time_calls(lambda i: graph.replay(), 5)
+        gpt2["graph_ms_per_decode_step"] = round(graph_ms / steps2, 5)
+        gpt2["graph_tokens_per_s_per_layer"] = round(S2 / (graph_ms / steps2 / L2n / 1e3), 1)
+        del graph
+    except Exception as exc:   # capture is an optional view of the same work
+        gpt2["graph_error"] = str(exc)[:200]
+    del k2, v2, pool2
 
     clocks = sampler.stop()
-    fp32_peak = props.multi_processor_count * 128 * 2 * (clocks.get("sm_max_mhz") or 2070.0) * 1e6 / 1e12
+    tc_peak, tc_src = read_tensor_peak()
     status = pkv.pf_device_status(reset=True)
     if status:
         raise RuntimeError(f"device status word {status} after the timed runs")
@@ -626,15 +749,21 @@ def run_ours(args, dist):
                              "without_workspace_ms": round(app2_ms, 5),
                              "without_workspace_gbs": round(app_bytes / (app2_ms / 1e3) / 1e9, 1)},
         "prompt_prefill": {"prompts": Sp, "tokens": Lp, "ms": round(pr_ms, 4), "flops": pr_flops,
-                           "tflops": round(pr_flops / (pr_ms / 1e3) / 1e12, 2), "bound": "alu",
-                           "fp32_fma_peak_tflops": round(fp32_peak, 1),
-                           "frac": round(pr_flops / (pr_ms / 1e3) / 1e12 / fp32_peak, 4),
-                           "peak_note": "SMs x 128 fp32 lanes x 2 flop x max SM clock (CUDA cores, no tensor cores)"},
+                           "tflops": round(pr_flops / (pr_ms / 1e3) / 1e12, 2), "bound": "tensor",
+                           "peak_tflops": tc_peak,
+                           "frac": round(pr_flops / (pr_ms / 1e3) / 1e12 / tc_peak, 4),
+                           "kernel": "prefill_mma_kernel<64> (mma.sync m16n8k16 fp16, fp32 accumulate)",
+                           "peak_note": f"{tc_src} dense bf16 burst TFLOP/s (MEASURED_PEAKS.json bf16_tflops; fp16 "
+                                        "has the same nominal rate)"},
         "gqa_attention": {"workload": "256 sequences of U[32,4096] tokens, 14 q-heads / 2 kv-heads x 64, "
                                       "block 16, shuffled frames", "kernel": "paged_decode_kernel_mma_r128<64,8,2> "
                                       "(7 rows per kv-head on tensor cores)", "ms": round(gqa_ms, 5), "bytes": gqa_bytes,
                           "gbs": round(gqa_bytes / (gqa_ms / 1e3) / 1e9, 1),
                           "frac_of_measured_copy": round(gqa_bytes / (gqa_ms / 1e3) / 1e9 / peak, 4)},
+        "gqa_block_sizes": gqa_sweep,
+        "split_13b": {"workload": "40 heads x 128, 2048 tokens per sequence, block 16, shuffled frames",
+                      "rows": split13},
+        "decode_loop_gpt2": gpt2,
         "gather": {"gbs": round(g_bytes / (gather_ms / 1e3) / 1e9, 1), "ms": round(gather_ms, 5),
                    "bytes": g_bytes, "frac_of_measured_copy": round(g_bytes / (gather_ms / 1e3) / 1e9 / peak, 4)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",

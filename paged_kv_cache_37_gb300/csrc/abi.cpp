@@ -348,8 +348,8 @@ int pf_paged_prefill_attention(const pf_pool *pool, int layer, const void *q, co
     if (n_q_heads <= 0 || n_q_heads % pool->n_kv_heads)
         return pkv::set_error(PF_ERR_INVALID,
                               "pf_paged_prefill_attention: n_q_heads must be a positive multiple of n_kv_heads");
-    if (n_q_heads / pool->n_kv_heads > 8)
-        return pkv::set_error(PF_ERR_UNSUPPORTED, "pf_paged_prefill_attention: at most 8 q-heads per kv-head are built");
+    if (n_q_heads / pool->n_kv_heads > 16)
+        return pkv::set_error(PF_ERR_UNSUPPORTED, "pf_paged_prefill_attention: at most 16 q-heads per kv-head are built");
     if (max_blocks_per_seq <= 0 || (long long)max_blocks_per_seq * pool->block_size > (1ll << 30))
         return pkv::set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: bad max_blocks_per_seq");
     if (!(scale > 0.0f) || scale != scale)

@@ -103,7 +103,7 @@ struct PrefillArgs {
     void *out;
     int out_dtype;
 };
-int launch_prefill(const PrefillArgs &a, cudaStream_t stream);
+int launch_prefill(const PrefillArgs &a, cudaStream_t stream);   // prefill_mma.cu
 
 struct GatherArgs {
     const pf_pool *pool;

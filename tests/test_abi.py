@@ -114,11 +114,11 @@ def test_device_calls_reject_bad_arguments_before_launch(pkv):
     assert lib.pf_swap_out(pool, ok, 2, P(0x30008), None) == pkv.PF_ERR_INVALID      # not 16-byte aligned
     assert lib.pf_swap_in(pool, ok, ok, -3, None) == pkv.PF_ERR_INVALID
     assert lib.pf_swap_in(pool, None, None, 0, None) == pkv.PF_OK
-    # prefill: q-heads not a multiple, group > 8, unaligned q, negative counts; no new token is a no-op
+    # prefill: q-heads not a multiple, group > 16, unaligned q, negative counts; no new token is a no-op
     pre = lambda hq=12, qp=ok, n=4, mx=3, dt=1: (pool, 0, qp, ok, 7, ok, ok, n, mx, hq, ctypes.c_float(0.125), ok,
                                                  dt, None, 0, None)
     assert lib.pf_paged_prefill_attention(*pre(hq=13)) == pkv.PF_ERR_INVALID
-    assert lib.pf_paged_prefill_attention(*pre(hq=12 * 9)) == pkv.PF_ERR_UNSUPPORTED
+    assert lib.pf_paged_prefill_attention(*pre(hq=12 * 17)) == pkv.PF_ERR_UNSUPPORTED
     assert lib.pf_paged_prefill_attention(*pre(qp=P(0x30004))) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_prefill_attention(*pre(n=-1)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_prefill_attention(*pre(dt=7)) == pkv.PF_ERR_INVALID
