@@ -63,6 +63,8 @@ def parse_args(argv=None):
     p.add_argument("--split", type=int, default=0, help="split_tokens (0 auto, -1 never)")
     p.add_argument("--cpu-budget-s", type=float, default=10.0, help="seconds of oracle work for cpu_baseline")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--main-only", action="store_true",
+                   help="time the decode step legs only (no side legs): the command profiles are taken with")
     return p.parse_args(argv)
 
 
@@ -417,228 +419,270 @@ def run_ours(args, dist):
     attn_ms = dist.max(per_unf["attn_ms"])
     write_ms = dist.max(per_unf["write_ms"])
 
-    # gather leg: rebuild contiguous K/V for the whole batch
-    off = si.cu_offsets(lens)
-    T = int(off[-1])
-    off_d = to(off[:-1])
-    outs = [(torch.empty((T, Hkv, D), dtype=torch.float16, device=device),
-             torch.empty((T, Hkv, D), dtype=torch.float16, device=device)) for _ in range(R)]
-    g_args = [(reps[r]["pool"].handle, 0, P(tables["shuffled"]), maxb, P(lens_d), P(off_d), S,
-               P(outs[r][0]), P(outs[r][1]), sp) for r in range(R)]
-    for i in range(W):
-        check(lib.pf_gather_kv(*g_args[i % R]))
-    Kg = max(10, K // 10)
-    dist.barrier()
-    torch.cuda.synchronize(device)
-    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    g0.record(stream)
-    for i in range(Kg):
-        check(lib.pf_gather_kv(*g_args[i % R]))
-    g1.record(stream)
-    torch.cuda.synchronize(device)
-    gather_ms = dist.max(g0.elapsed_time(g1) / Kg)
-    g_bytes = gather_bytes(lens, Hkv, D, B)
-    del outs
-
-    # whole-block legs: copy-on-write copies inside a pool (half the pool's
-    # blocks onto the other half) and swapping the same blocks out to pinned
-    # host memory and back in; bytes = every image read once and written once
-    img = pkv.pf_block_image_bytes(reps[0]["pool"])
-    nb = w["n_blocks"] // 2
-    src_ids = to(np.arange(nb, dtype=np.int32))
-    dst_ids = to(np.arange(nb, 2 * nb, dtype=np.int32))
-    blk_bytes = 2 * nb * img
-    swap_buf = torch.empty(nb * img, dtype=torch.uint8).pin_memory()
-
-    def time_calls(fn, n):
-        for i in range(3):
-            fn(i)
+    # side legs (skipped with --main-only, e.g. under a profiler)
+    peak, peak_src = read_peaks()
+    tc_peak, tc_src = read_tensor_peak()
+    side = {}
+    if not args.main_only:
+        # gather leg: rebuild contiguous K/V for the whole batch
+        off = si.cu_offsets(lens)
+        T = int(off[-1])
+        off_d = to(off[:-1])
+        outs = [(torch.empty((T, Hkv, D), dtype=torch.float16, device=device),
+                 torch.empty((T, Hkv, D), dtype=torch.float16, device=device)) for _ in range(R)]
+        g_args = [(reps[r]["pool"].handle, 0, P(tables["shuffled"]), maxb, P(lens_d), P(off_d), S,
+                   P(outs[r][0]), P(outs[r][1]), sp) for r in range(R)]
+        for i in range(W):
+            check(lib.pf_gather_kv(*g_args[i % R]))
+        Kg = max(10, K // 10)
         dist.barrier()
         torch.cuda.synchronize(device)
-        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        b0.record(stream)
-        for i in range(n):
-            fn(i)
-        b1.record(stream)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for i in range(Kg):
+            check(lib.pf_gather_kv(*g_args[i % R]))
+        g1.record(stream)
         torch.cuda.synchronize(device)
-        return dist.max(b0.elapsed_time(b1) / n)
+        gather_ms = dist.max(g0.elapsed_time(g1) / Kg)
+        g_bytes = gather_bytes(lens, Hkv, D, B)
+        del outs
 
-    copy_ms = time_calls(lambda i: check(lib.pf_copy_blocks(reps[i % R]["pool"].handle, P(src_ids), P(dst_ids),
-                                                             nb, sp)), Kg)
-    swap_out_ms = time_calls(lambda i: check(lib.pf_swap_out(reps[i % R]["pool"].handle, P(src_ids), nb,
-                                                              P(swap_buf), sp)), 10)
-    swap_in_ms = time_calls(lambda i: check(lib.pf_swap_in(reps[i % R]["pool"].handle, P(swap_buf), P(dst_ids),
-                                                            nb, sp)), 10)
-    # the platform's own rate for the same bytes: copy-engine copies between
-    # device memory and the same pinned buffer
-    ce_dev = torch.empty(nb * img, dtype=torch.uint8, device=device)
-    ce_d2h_ms = time_calls(lambda i: swap_buf.copy_(ce_dev, non_blocking=True), 10)
-    ce_h2d_ms = time_calls(lambda i: ce_dev.copy_(swap_buf, non_blocking=True), 10)
-    del swap_buf, ce_dev
+        # whole-block legs: copy-on-write copies inside a pool (half the pool's
+        # blocks onto the other half) and swapping the same blocks out to pinned
+        # host memory and back in; bytes = every image read once and written once
+        img = pkv.pf_block_image_bytes(reps[0]["pool"])
+        nb = w["n_blocks"] // 2
+        src_ids = to(np.arange(nb, dtype=np.int32))
+        dst_ids = to(np.arange(nb, 2 * nb, dtype=np.int32))
+        blk_bytes = 2 * nb * img
+        swap_buf = torch.empty(nb * img, dtype=torch.uint8).pin_memory()
 
-    # multi-token append legs.  (1) 8 new tokens at the end of every sequence
-    # of the workload (each sequence's K/V read once per kv-head: HBM-bound);
-    # (2) whole prompts, 4 x 2048 tokens (causal attention over each prompt:
-    # fp32 FMA-bound on the CUDA cores)
-    n_app = 8
-    cu_app = to(np.arange(S + 1, dtype=np.int32) * n_app)
-    q_app = torch.randn((S * n_app, Hq, D), device=device).half()
-    o_app = torch.empty_like(q_app)
-    # the decode kernel takes it (8 tokens x 1 q-head = 8 rows per kv-head)
-    app_ws = [pkv.make_prefill_workspace(reps[r]["pool"], S, Hq, maxb, n_app) for r in range(R)]
-    app_args = [(reps[r]["pool"].handle, 0, P(q_app), P(tables["shuffled"]), maxb, P(lens_d), P(cu_app), S, n_app,
-                 Hq, ctypes.c_float(w["scale"]), P(o_app), pkv.PF_F16, P(app_ws[r]), app_ws[r].numel(), sp)
-                for r in range(R)]
-    app_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*app_args[i % R])), Kg)
-    # the same append through the kernel that needs no workspace
-    app2_args = [a_[:13] + (None, 0, sp) for a_ in app_args]
-    app2_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*app2_args[i % R])), Kg)
-    del app_ws
-    app_bytes = attention_bytes(lens, Hq, Hkv, D, B) + (n_app - 1) * S * Hq * D * 2 * 2 + 4 * (S + 1)
-    Lp, Sp = 2048, 4
-    pr_lens = to(np.full(Sp, Lp, dtype=np.int32))
-    pr_bt = to(np.arange(Sp * Lp // B, dtype=np.int32).reshape(Sp, Lp // B))
-    pr_cu = to(np.arange(Sp + 1, dtype=np.int32) * Lp)
-    q_pr = torch.randn((Sp * Lp, Hq, D), device=device).half()
-    o_pr = torch.empty_like(q_pr)
-    pr_args = (reps[0]["pool"].handle, 0, P(q_pr), P(pr_bt), Lp // B, P(pr_lens), P(pr_cu), Sp, Lp, Hq,
-               ctypes.c_float(w["scale"]), P(o_pr), pkv.PF_F16, None, 0, sp)
-    pr_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*pr_args)), 10)
-    pr_flops = 4.0 * Hq * D * Sp * Lp * (Lp + 1) / 2        # q.k and p.v over every causal pair
-    del q_app, o_app, q_pr, o_pr
+        def time_calls(fn, n):
+            for i in range(3):
+                fn(i)
+            dist.barrier()
+            torch.cuda.synchronize(device)
+            b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            b0.record(stream)
+            for i in range(n):
+                fn(i)
+            b1.record(stream)
+            torch.cuda.synchronize(device)
+            return dist.max(b0.elapsed_time(b1) / n)
 
-    # grouped heads: 14 q-heads over 2 kv-heads x 64, 256 sequences of
-    # U[32, 4096] tokens (each K/V byte serves 7 q-heads), attention alone
-    wg = si.WORKLOADS["gqa"]
-    g_lens = si.uniform_lengths(wg["n_seqs"], wg["len_lo"], wg["len_hi"], seed=12)
-    gHq, gHkv, gD, gB = wg["n_q_heads"], wg["n_kv_heads"], wg["head_dim"], 16
-    gN = int(sum(-(-int(L_) // gB) for L_ in g_lens)) + 64
-    g_maxb = -(-int(g_lens.max()) // gB)
-    g_bt = to(si.block_tables(g_lens, gB, gN, si.SEED_SHUFFLE, max_blocks=g_maxb))
-    g_lens_d = to(g_lens)
-    g_reps = []
-    for r in range(2):
-        gk = torch.empty((1, gN, gB, gHkv, gD), dtype=torch.float16, device=device).normal_()
-        gv = torch.empty_like(gk).normal_()
-        gpool = pkv.pf_pool_create(gk, gv)
-        gq = torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device).normal_()
-        g_reps.append((gk, gv, gpool, gq, torch.empty_like(gq), pkv.make_workspace(gpool, wg["n_seqs"], gHq, g_maxb)))
-    g_args = [(gr[2].handle, 0, P(gr[3]), P(g_bt), g_maxb, P(g_lens_d), wg["n_seqs"], gHq, ctypes.c_float(wg["scale"]),
-               P(gr[4]), pkv.PF_F16, 0, P(gr[5]), gr[5].numel(), sp) for gr in g_reps]
-    gqa_ms = time_calls(lambda i: check(lib.pf_paged_decode_attention(*g_args[i % 2])), Kg)
-    gqa_bytes = attention_bytes(g_lens, gHq, gHkv, gD, gB)
-    del g_reps
-    # the same token counts stored in pages of 1, 64 and 256 tokens
-    gqa_sweep = [{"block_size": gB, "ms": round(gqa_ms, 5), "gbs": round(gqa_bytes / (gqa_ms / 1e3) / 1e9, 1)}]
-    for bs in (1, 64, 256):
-        sN = int(sum(-(-int(L_) // bs) for L_ in g_lens)) + 64
-        s_maxb = -(-int(g_lens.max()) // bs)
-        s_bt = to(si.block_tables(g_lens, bs, sN, si.SEED_SHUFFLE, max_blocks=s_maxb))
-        s_reps = []
+        copy_ms = time_calls(lambda i: check(lib.pf_copy_blocks(reps[i % R]["pool"].handle, P(src_ids), P(dst_ids),
+                                                                 nb, sp)), Kg)
+        swap_out_ms = time_calls(lambda i: check(lib.pf_swap_out(reps[i % R]["pool"].handle, P(src_ids), nb,
+                                                                  P(swap_buf), sp)), 10)
+        swap_in_ms = time_calls(lambda i: check(lib.pf_swap_in(reps[i % R]["pool"].handle, P(swap_buf), P(dst_ids),
+                                                                nb, sp)), 10)
+        # the platform's own rate for the same bytes: copy-engine copies between
+        # device memory and the same pinned buffer
+        ce_dev = torch.empty(nb * img, dtype=torch.uint8, device=device)
+        ce_d2h_ms = time_calls(lambda i: swap_buf.copy_(ce_dev, non_blocking=True), 10)
+        ce_h2d_ms = time_calls(lambda i: ce_dev.copy_(swap_buf, non_blocking=True), 10)
+        del swap_buf, ce_dev
+
+        # multi-token append legs.  (1) 8 new tokens at the end of every sequence
+        # of the workload (each sequence's K/V read once per kv-head: HBM-bound);
+        # (2) whole prompts, 4 x 2048 tokens (causal attention over each prompt:
+        # fp32 FMA-bound on the CUDA cores)
+        n_app = 8
+        cu_app = to(np.arange(S + 1, dtype=np.int32) * n_app)
+        q_app = torch.randn((S * n_app, Hq, D), device=device).half()
+        o_app = torch.empty_like(q_app)
+        # the decode kernel takes it (8 tokens x 1 q-head = 8 rows per kv-head)
+        app_ws = [pkv.make_prefill_workspace(reps[r]["pool"], S, Hq, maxb, n_app) for r in range(R)]
+        app_args = [(reps[r]["pool"].handle, 0, P(q_app), P(tables["shuffled"]), maxb, P(lens_d), P(cu_app), S, n_app,
+                     Hq, ctypes.c_float(w["scale"]), P(o_app), pkv.PF_F16, P(app_ws[r]), app_ws[r].numel(), sp)
+                    for r in range(R)]
+        app_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*app_args[i % R])), Kg)
+        # the same append through the kernel that needs no workspace
+        app2_args = [a_[:13] + (None, 0, sp) for a_ in app_args]
+        app2_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*app2_args[i % R])), Kg)
+        del app_ws
+        app_bytes = attention_bytes(lens, Hq, Hkv, D, B) + (n_app - 1) * S * Hq * D * 2 * 2 + 4 * (S + 1)
+        Lp, Sp = 2048, 4
+        pr_lens = to(np.full(Sp, Lp, dtype=np.int32))
+        pr_bt = to(np.arange(Sp * Lp // B, dtype=np.int32).reshape(Sp, Lp // B))
+        pr_cu = to(np.arange(Sp + 1, dtype=np.int32) * Lp)
+        q_pr = torch.randn((Sp * Lp, Hq, D), device=device).half()
+        o_pr = torch.empty_like(q_pr)
+        pr_args = (reps[0]["pool"].handle, 0, P(q_pr), P(pr_bt), Lp // B, P(pr_lens), P(pr_cu), Sp, Lp, Hq,
+                   ctypes.c_float(w["scale"]), P(o_pr), pkv.PF_F16, None, 0, sp)
+        pr_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*pr_args)), 10)
+        pr_flops = 4.0 * Hq * D * Sp * Lp * (Lp + 1) / 2        # q.k and p.v over every causal pair
+        del q_app, o_app, q_pr, o_pr
+
+        # grouped heads: 14 q-heads over 2 kv-heads x 64, 256 sequences of
+        # U[32, 4096] tokens (each K/V byte serves 7 q-heads), attention alone
+        wg = si.WORKLOADS["gqa"]
+        g_lens = si.uniform_lengths(wg["n_seqs"], wg["len_lo"], wg["len_hi"], seed=12)
+        gHq, gHkv, gD, gB = wg["n_q_heads"], wg["n_kv_heads"], wg["head_dim"], 16
+        gN = int(sum(-(-int(L_) // gB) for L_ in g_lens)) + 64
+        g_maxb = -(-int(g_lens.max()) // gB)
+        g_bt = to(si.block_tables(g_lens, gB, gN, si.SEED_SHUFFLE, max_blocks=g_maxb))
+        g_lens_d = to(g_lens)
+        g_reps = []
         for r in range(2):
-            sk = torch.empty((1, sN, bs, gHkv, gD), dtype=torch.float16, device=device).normal_()
-            sv = torch.empty_like(sk).normal_()
-            spool = pkv.pf_pool_create(sk, sv)
-            s_reps.append((sk, sv, spool, pkv.make_workspace(spool, wg["n_seqs"], gHq, s_maxb),
-                           torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device)))
-        gq0 = torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device).normal_()
-        s_args = [(sr[2].handle, 0, P(gq0), P(s_bt), s_maxb, P(g_lens_d), wg["n_seqs"], gHq,
-                   ctypes.c_float(wg["scale"]), P(sr[4]), pkv.PF_F16, 0, P(sr[3]), sr[3].numel(), sp) for sr in s_reps]
-        s_ms = time_calls(lambda i: check(lib.pf_paged_decode_attention(*s_args[i % 2])), max(10, Kg // 4))
-        s_bytes = attention_bytes(g_lens, gHq, gHkv, gD, bs)
-        gqa_sweep.append({"block_size": bs, "ms": round(s_ms, 5), "gbs": round(s_bytes / (s_ms / 1e3) / 1e9, 1)})
-        del s_reps, gq0
+            gk = torch.empty((1, gN, gB, gHkv, gD), dtype=torch.float16, device=device).normal_()
+            gv = torch.empty_like(gk).normal_()
+            gpool = pkv.pf_pool_create(gk, gv)
+            gq = torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device).normal_()
+            g_reps.append((gk, gv, gpool, gq, torch.empty_like(gq), pkv.make_workspace(gpool, wg["n_seqs"], gHq, g_maxb)))
+        g_args = [(gr[2].handle, 0, P(gr[3]), P(g_bt), g_maxb, P(g_lens_d), wg["n_seqs"], gHq, ctypes.c_float(wg["scale"]),
+                   P(gr[4]), pkv.PF_F16, 0, P(gr[5]), gr[5].numel(), sp) for gr in g_reps]
+        gqa_ms = time_calls(lambda i: check(lib.pf_paged_decode_attention(*g_args[i % 2])), Kg)
+        gqa_bytes = attention_bytes(g_lens, gHq, gHkv, gD, gB)
+        del g_reps
+        # the same token counts stored in pages of 1, 64 and 256 tokens
+        gqa_sweep = [{"block_size": gB, "ms": round(gqa_ms, 5), "gbs": round(gqa_bytes / (gqa_ms / 1e3) / 1e9, 1)}]
+        for bs in (1, 64, 256):
+            sN = int(sum(-(-int(L_) // bs) for L_ in g_lens)) + 64
+            s_maxb = -(-int(g_lens.max()) // bs)
+            s_bt = to(si.block_tables(g_lens, bs, sN, si.SEED_SHUFFLE, max_blocks=s_maxb))
+            s_reps = []
+            for r in range(2):
+                sk = torch.empty((1, sN, bs, gHkv, gD), dtype=torch.float16, device=device).normal_()
+                sv = torch.empty_like(sk).normal_()
+                spool = pkv.pf_pool_create(sk, sv)
+                s_reps.append((sk, sv, spool, pkv.make_workspace(spool, wg["n_seqs"], gHq, s_maxb),
+                               torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device)))
+            gq0 = torch.empty((wg["n_seqs"], gHq, gD), dtype=torch.float16, device=device).normal_()
+            s_args = [(sr[2].handle, 0, P(gq0), P(s_bt), s_maxb, P(g_lens_d), wg["n_seqs"], gHq,
+                       ctypes.c_float(wg["scale"]), P(sr[4]), pkv.PF_F16, 0, P(sr[3]), sr[3].numel(), sp) for sr in s_reps]
+            s_ms = time_calls(lambda i: check(lib.pf_paged_decode_attention(*s_args[i % 2])), max(10, Kg // 4))
+            s_bytes = attention_bytes(g_lens, gHq, gHkv, gD, bs)
+            gqa_sweep.append({"block_size": bs, "ms": round(s_ms, 5), "gbs": round(s_bytes / (s_ms / 1e3) / 1e9, 1)})
+            del s_reps, gq0
 
-    # 13B-like: 40 heads x 128, every sequence at 2048 tokens, batch 1 .. 64,
-    # the balanced schedule (split_tokens 0) against no split (-1).  One pool
-    # of 64 x 128 pages; a batch of S rotates over 64 / S disjoint table sets,
-    # so no call finds its pages in L2.
-    w13 = si.WORKLOADS["13b"]
-    c13, H13, D13, B13 = w13["context_len"], w13["n_q_heads"], w13["head_dim"], w13["block_size"]
-    pages13 = c13 // B13
-    N13 = 64 * pages13
-    k13 = torch.empty((1, N13, B13, H13, D13), dtype=torch.float16, device=device).normal_()
-    v13 = torch.empty_like(k13).normal_()
-    pool13 = pkv.pf_pool_create(k13, v13)
-    bt13 = si.block_tables(np.full(64, c13, dtype=np.int32), B13, N13, si.SEED_SHUFFLE, max_blocks=pages13)
-    split13 = []
-    for S13 in w13["batches"]:
-        sets = 64 // S13
-        tabs = [to(np.ascontiguousarray(bt13[j * S13:(j + 1) * S13])) for j in range(sets)]
-        l13 = to(np.full(S13, c13, dtype=np.int32))
-        q13 = torch.empty((S13, H13, D13), dtype=torch.float16, device=device).normal_()
-        o13 = torch.empty_like(q13)
-        row = {"batch": S13}
-        b13 = attention_bytes(np.full(S13, c13), H13, H13, D13, B13)
-        for name_, spl in (("balanced", 0), ("no_split", -1)):
-            ws13 = pkv.make_workspace(pool13, S13, H13, pages13, spl)
-            a13 = [(pool13.handle, 0, P(q13), P(t_), pages13, P(l13), S13, H13, ctypes.c_float(w13["scale"]),
-                    P(o13), pkv.PF_F16, spl, P(ws13), ws13.numel(), sp) for t_ in tabs]
-            ms13 = time_calls(lambda i: check(lib.pf_paged_decode_attention(*a13[i % sets])), 20)
-            row[name_ + "_us"] = round(ms13 * 1e3, 2)
-            row[name_ + "_gbs"] = round(b13 / (ms13 / 1e3) / 1e9, 1)
-        split13.append(row)
-    del k13, v13, pool13
+        # 13B-like: 40 heads x 128, every sequence at 2048 tokens, batch 1 .. 64,
+        # the balanced schedule (split_tokens 0) against no split (-1).  One pool
+        # of 64 x 128 pages; a batch of S rotates over 64 / S disjoint table sets,
+        # so no call finds its pages in L2.
+        w13 = si.WORKLOADS["13b"]
+        c13, H13, D13, B13 = w13["context_len"], w13["n_q_heads"], w13["head_dim"], w13["block_size"]
+        pages13 = c13 // B13
+        N13 = 64 * pages13
+        k13 = torch.empty((1, N13, B13, H13, D13), dtype=torch.float16, device=device).normal_()
+        v13 = torch.empty_like(k13).normal_()
+        pool13 = pkv.pf_pool_create(k13, v13)
+        bt13 = si.block_tables(np.full(64, c13, dtype=np.int32), B13, N13, si.SEED_SHUFFLE, max_blocks=pages13)
+        split13 = []
+        for S13 in w13["batches"]:
+            sets = 64 // S13
+            tabs = [to(np.ascontiguousarray(bt13[j * S13:(j + 1) * S13])) for j in range(sets)]
+            l13 = to(np.full(S13, c13, dtype=np.int32))
+            q13 = torch.empty((S13, H13, D13), dtype=torch.float16, device=device).normal_()
+            o13 = torch.empty_like(q13)
+            row = {"batch": S13}
+            b13 = attention_bytes(np.full(S13, c13), H13, H13, D13, B13)
+            for name_, spl in (("balanced", 0), ("no_split", -1)):
+                ws13 = pkv.make_workspace(pool13, S13, H13, pages13, spl)
+                a13 = [(pool13.handle, 0, P(q13), P(t_), pages13, P(l13), S13, H13, ctypes.c_float(w13["scale"]),
+                        P(o13), pkv.PF_F16, spl, P(ws13), ws13.numel(), sp) for t_ in tabs]
+                ms13 = time_calls(lambda i: check(lib.pf_paged_decode_attention(*a13[i % sets])), 20)
+                row[name_ + "_us"] = round(ms13 * 1e3, 2)
+                row[name_ + "_gbs"] = round(b13 / (ms13 / 1e3) / 1e9, 1)
+            split13.append(row)
+        del k13, v13, pool13
 
-    # GPT-2-shaped decode loop: 12 layers x 12 heads x 64, 32 sequences with
-    # prompts of U[16, 64] tokens, 50 decode steps of one fused call per
-    # layer (launch-bound: ~9 MB per layer call).  Pages for the final
-    # lengths are allocated up front; step i attends over prompt + i + 1.
-    w2 = si.WORKLOADS["gpt2"]
-    S2, L2n, H2, D2, B2 = w2["n_seqs"], w2["n_layers"], w2["n_q_heads"], w2["head_dim"], w2["block_size"]
-    steps2 = w2["decode_steps"]
-    pr2 = si.uniform_lengths(S2, w2["prompt_lo"], w2["prompt_hi"])
-    N2 = S2 * w2["tokens_per_seq"] // B2
-    maxb2 = w2["tokens_per_seq"] // B2
-    bt2 = to(si.block_tables(pr2 + steps2, B2, N2, si.SEED_SHUFFLE, max_blocks=maxb2))
-    lens2 = to(np.stack([pr2 + i + 1 for i in range(steps2)]).astype(np.int32))
-    k2 = torch.empty((L2n, N2, B2, H2, D2), dtype=torch.float16, device=device).normal_()
-    v2 = torch.empty_like(k2).normal_()
-    pool2 = pkv.pf_pool_create(k2, v2)
-    q2 = torch.empty((L2n, S2, H2, D2), dtype=torch.float16, device=device).normal_()
-    kn2 = torch.empty((L2n, S2, H2, D2), dtype=torch.float16, device=device).normal_()
-    o2 = torch.empty_like(q2)
-    ws2 = pkv.make_workspace(pool2, S2, H2, maxb2, 0)
-    args2 = [[(pool2.handle, l_, P(q2[l_]), P(kn2[l_]), P(kn2[l_]), P(bt2), maxb2, P(lens2[i]), S2, H2,
-               ctypes.c_float(w2["scale"]), P(o2[l_]), pkv.PF_F16, 0, P(ws2), ws2.numel(),
-               pkv.PF_STEP_OVERLAP_PREVIOUS, sp) for l_ in range(L2n)] for i in range(steps2)]
+        # GPT-2-shaped decode loop: 12 layers x 12 heads x 64, 32 sequences with
+        # prompts of U[16, 64] tokens, 50 decode steps of one fused call per
+        # layer (launch-bound: ~9 MB per layer call).  Pages for the final
+        # lengths are allocated up front; step i attends over prompt + i + 1.
+        w2 = si.WORKLOADS["gpt2"]
+        S2, L2n, H2, D2, B2 = w2["n_seqs"], w2["n_layers"], w2["n_q_heads"], w2["head_dim"], w2["block_size"]
+        steps2 = w2["decode_steps"]
+        pr2 = si.uniform_lengths(S2, w2["prompt_lo"], w2["prompt_hi"])
+        N2 = S2 * w2["tokens_per_seq"] // B2
+        maxb2 = w2["tokens_per_seq"] // B2
+        bt2 = to(si.block_tables(pr2 + steps2, B2, N2, si.SEED_SHUFFLE, max_blocks=maxb2))
+        lens2 = to(np.stack([pr2 + i + 1 for i in range(steps2)]).astype(np.int32))
+        k2 = torch.empty((L2n, N2, B2, H2, D2), dtype=torch.float16, device=device).normal_()
+        v2 = torch.empty_like(k2).normal_()
+        pool2 = pkv.pf_pool_create(k2, v2)
+        q2 = torch.empty((L2n, S2, H2, D2), dtype=torch.float16, device=device).normal_()
+        kn2 = torch.empty((L2n, S2, H2, D2), dtype=torch.float16, device=device).normal_()
+        o2 = torch.empty_like(q2)
+        ws2 = pkv.make_workspace(pool2, S2, H2, maxb2, 0)
+        args2 = [[(pool2.handle, l_, P(q2[l_]), P(kn2[l_]), P(kn2[l_]), P(bt2), maxb2, P(lens2[i]), S2, H2,
+                   ctypes.c_float(w2["scale"]), P(o2[l_]), pkv.PF_F16, 0, P(ws2), ws2.numel(),
+                   pkv.PF_STEP_OVERLAP_PREVIOUS, sp) for l_ in range(L2n)] for i in range(steps2)]
 
-    def decode_loop(_):
-        for i in range(steps2):
-            for l_ in range(L2n):
-                check(lib.pf_decode_step(*args2[i][l_]))
-
-    loop_ms = time_calls(decode_loop, 5)
-    bytes2 = sum(attention_bytes(pr2 + i + 1, H2, H2, D2, B2) + write_bytes(S2, H2, D2) for i in range(steps2)) * L2n
-    gpt2 = {"workload": "12 layers x 12 heads x 64, 32 sequences, prompts U[16,64], 50 decode steps, block 16, "
-                        "pool of 512 tokens per sequence, shuffled frames",
-            "ms_per_decode_step": round(loop_ms / steps2, 5),
-            "us_per_layer_call": round(loop_ms / steps2 / L2n * 1e3, 2),
-            "tokens_per_s_per_layer": round(S2 / (loop_ms / steps2 / L2n / 1e3), 1),
-            "gbs": round(bytes2 / (loop_ms / 1e3) / 1e9, 1)}
-    # the same 600 calls replayed from a CUDA graph (launch cost removed)
-    try:
-        gstream = torch.cuda.Stream(device)
-        graph = torch.cuda.CUDAGraph()
-        gsp = ctypes.c_void_p(gstream.cuda_stream)
-        gargs = [[a_[:-1] + (gsp,) for a_ in row_] for row_ in args2]
-        with torch.cuda.stream(gstream):
-            decode_loop(0)   # warm on the capture stream
-        torch.cuda.synchronize(device)
-        with torch.cuda.graph(graph, stream=gstream):
+        def decode_loop(_):
             for i in range(steps2):
                 for l_ in range(L2n):
-                    check(lib.pf_decode_step(*gargs[i][l_]))
-        graph_ms = time_calls(lambda i: graph.replay(), 5)
-        gpt2["graph_ms_per_decode_step"] = round(graph_ms / steps2, 5)
-        gpt2["graph_tokens_per_s_per_layer"] = round(S2 / (graph_ms / steps2 / L2n / 1e3), 1)
-        del graph
-    except Exception as exc:   # capture is an optional view of the same work
-        gpt2["graph_error"] = str(exc)[:200]
-    del k2, v2, pool2
+                    check(lib.pf_decode_step(*args2[i][l_]))
 
+        loop_ms = time_calls(decode_loop, 5)
+        bytes2 = sum(attention_bytes(pr2 + i + 1, H2, H2, D2, B2) + write_bytes(S2, H2, D2) for i in range(steps2)) * L2n
+        gpt2 = {"workload": "12 layers x 12 heads x 64, 32 sequences, prompts U[16,64], 50 decode steps, block 16, "
+                            "pool of 512 tokens per sequence, shuffled frames",
+                "ms_per_decode_step": round(loop_ms / steps2, 5),
+                "us_per_layer_call": round(loop_ms / steps2 / L2n * 1e3, 2),
+                "tokens_per_s_per_layer": round(S2 / (loop_ms / steps2 / L2n / 1e3), 1),
+                "gbs": round(bytes2 / (loop_ms / 1e3) / 1e9, 1)}
+        # the same 600 calls replayed from a CUDA graph (launch cost removed)
+        try:
+            gstream = torch.cuda.Stream(device)
+            graph = torch.cuda.CUDAGraph()
+            gsp = ctypes.c_void_p(gstream.cuda_stream)
+            gargs = [[a_[:-1] + (gsp,) for a_ in row_] for row_ in args2]
+            with torch.cuda.stream(gstream):
+                decode_loop(0)   # warm on the capture stream
+            torch.cuda.synchronize(device)
+            with torch.cuda.graph(graph, stream=gstream):
+                for i in range(steps2):
+                    for l_ in range(L2n):
+                        check(lib.pf_decode_step(*gargs[i][l_]))
+            graph_ms = time_calls(lambda i: graph.replay(), 5)
+            gpt2["graph_ms_per_decode_step"] = round(graph_ms / steps2, 5)
+            gpt2["graph_tokens_per_s_per_layer"] = round(S2 / (graph_ms / steps2 / L2n / 1e3), 1)
+            del graph
+        except Exception as exc:   # capture is an optional view of the same work
+            gpt2["graph_error"] = str(exc)[:200]
+        del k2, v2, pool2
+
+        side = {
+            "block_copies": {"blocks": nb, "bytes": blk_bytes, "image_bytes": img,
+                             "copy_gbs": round(blk_bytes / (copy_ms / 1e3) / 1e9, 1), "copy_ms": round(copy_ms, 5),
+                             "copy_frac_of_measured_copy": round(blk_bytes / (copy_ms / 1e3) / 1e9 / peak, 4),
+                             "swap_out_gbs": round(blk_bytes / 2 / (swap_out_ms / 1e3) / 1e9, 1),
+                             "swap_in_gbs": round(blk_bytes / 2 / (swap_in_ms / 1e3) / 1e9, 1),
+                             "copy_engine_d2h_gbs": round(blk_bytes / 2 / (ce_d2h_ms / 1e3) / 1e9, 1),
+                             "copy_engine_h2d_gbs": round(blk_bytes / 2 / (ce_h2d_ms / 1e3) / 1e9, 1),
+                             "swap_out_frac_of_copy_engine": round(ce_d2h_ms / swap_out_ms, 4),
+                             "swap_in_frac_of_copy_engine": round(ce_h2d_ms / swap_in_ms, 4),
+                             "swap_note": "GB/s of images moved between HBM and page-locked host memory; the "
+                                          "copy engine's rate for the same bytes and buffer is the roofline"},
+            "append_attention": {"new_tokens_per_seq": n_app, "ms": round(app_ms, 5), "bytes": app_bytes,
+                                 "gbs": round(app_bytes / (app_ms / 1e3) / 1e9, 1),
+                                 "frac_of_measured_copy": round(app_bytes / (app_ms / 1e3) / 1e9 / peak, 4),
+                                 "kernel": "paged_decode_kernel_mma_r128<64,8,4> (8 rows per kv-head on tensor cores, "
+                                           "workspace path)",
+                                 "without_workspace_ms": round(app2_ms, 5),
+                                 "without_workspace_gbs": round(app_bytes / (app2_ms / 1e3) / 1e9, 1)},
+            "prompt_prefill": {"prompts": Sp, "tokens": Lp, "ms": round(pr_ms, 4), "flops": pr_flops,
+                               "tflops": round(pr_flops / (pr_ms / 1e3) / 1e12, 2), "bound": "tensor",
+                               "peak_tflops": tc_peak,
+                               "frac": round(pr_flops / (pr_ms / 1e3) / 1e12 / tc_peak, 4),
+                               "kernel": "prefill_mma_kernel<64> (mma.sync m16n8k16 fp16, fp32 accumulate)",
+                               "peak_note": f"{tc_src} dense bf16 burst TFLOP/s (MEASURED_PEAKS.json bf16_tflops; fp16 "
+                                            "has the same nominal rate)"},
+            "gqa_attention": {"workload": "256 sequences of U[32,4096] tokens, 14 q-heads / 2 kv-heads x 64, "
+                                          "block 16, shuffled frames", "kernel": "paged_decode_kernel_mma_r128<64,8,2> "
+                                          "(7 rows per kv-head on tensor cores)", "ms": round(gqa_ms, 5), "bytes": gqa_bytes,
+                              "gbs": round(gqa_bytes / (gqa_ms / 1e3) / 1e9, 1),
+                              "frac_of_measured_copy": round(gqa_bytes / (gqa_ms / 1e3) / 1e9 / peak, 4)},
+            "gqa_block_sizes": gqa_sweep,
+            "split_13b": {"workload": "40 heads x 128, 2048 tokens per sequence, block 16, shuffled frames",
+                          "rows": split13},
+            "decode_loop_gpt2": gpt2,
+            "gather": {"gbs": round(g_bytes / (gather_ms / 1e3) / 1e9, 1), "ms": round(gather_ms, 5),
+                       "bytes": g_bytes, "frac_of_measured_copy": round(g_bytes / (gather_ms / 1e3) / 1e9 / peak, 4)},
+        }
     clocks = sampler.stop()
-    tc_peak, tc_src = read_tensor_peak()
     status = pkv.pf_device_status(reset=True)
     if status:
         raise RuntimeError(f"device status word {status} after the timed runs")
@@ -693,7 +737,6 @@ def run_ours(args, dist):
                "ms_per_step": round(el * 1e3 / Ke, 4),
                "tokens_per_s_per_layer": round(dist.sum(S) * Ke / el, 1)}
 
-    peak, peak_src = read_peaks()
     step_s = ms_main / 1e3 / K
     call_s = step_call_ms / 1e3
     achieved = step_bytes / call_s / 1e9
@@ -730,45 +773,11 @@ def run_ours(args, dist):
         "ordered": {"ms_per_step": round(ms_ord / K, 5), "decode_step_ms": round(step_ord_ms, 5),
                     "gbs": round(step_bytes / (step_ord_ms / 1e3) / 1e9, 1),
                     "shuffled_over_ordered_time": round(step_call_ms / step_ord_ms, 4)},
-        "block_copies": {"blocks": nb, "bytes": blk_bytes, "image_bytes": img,
-                         "copy_gbs": round(blk_bytes / (copy_ms / 1e3) / 1e9, 1), "copy_ms": round(copy_ms, 5),
-                         "copy_frac_of_measured_copy": round(blk_bytes / (copy_ms / 1e3) / 1e9 / peak, 4),
-                         "swap_out_gbs": round(blk_bytes / 2 / (swap_out_ms / 1e3) / 1e9, 1),
-                         "swap_in_gbs": round(blk_bytes / 2 / (swap_in_ms / 1e3) / 1e9, 1),
-                         "copy_engine_d2h_gbs": round(blk_bytes / 2 / (ce_d2h_ms / 1e3) / 1e9, 1),
-                         "copy_engine_h2d_gbs": round(blk_bytes / 2 / (ce_h2d_ms / 1e3) / 1e9, 1),
-                         "swap_out_frac_of_copy_engine": round(ce_d2h_ms / swap_out_ms, 4),
-                         "swap_in_frac_of_copy_engine": round(ce_h2d_ms / swap_in_ms, 4),
-                         "swap_note": "GB/s of images moved between HBM and page-locked host memory; the "
-                                      "copy engine's rate for the same bytes and buffer is the roofline"},
-        "append_attention": {"new_tokens_per_seq": n_app, "ms": round(app_ms, 5), "bytes": app_bytes,
-                             "gbs": round(app_bytes / (app_ms / 1e3) / 1e9, 1),
-                             "frac_of_measured_copy": round(app_bytes / (app_ms / 1e3) / 1e9 / peak, 4),
-                             "kernel": "paged_decode_kernel_mma_r128<64,8,4> (8 rows per kv-head on tensor cores, "
-                                       "workspace path)",
-                             "without_workspace_ms": round(app2_ms, 5),
-                             "without_workspace_gbs": round(app_bytes / (app2_ms / 1e3) / 1e9, 1)},
-        "prompt_prefill": {"prompts": Sp, "tokens": Lp, "ms": round(pr_ms, 4), "flops": pr_flops,
-                           "tflops": round(pr_flops / (pr_ms / 1e3) / 1e12, 2), "bound": "tensor",
-                           "peak_tflops": tc_peak,
-                           "frac": round(pr_flops / (pr_ms / 1e3) / 1e12 / tc_peak, 4),
-                           "kernel": "prefill_mma_kernel<64> (mma.sync m16n8k16 fp16, fp32 accumulate)",
-                           "peak_note": f"{tc_src} dense bf16 burst TFLOP/s (MEASURED_PEAKS.json bf16_tflops; fp16 "
-                                        "has the same nominal rate)"},
-        "gqa_attention": {"workload": "256 sequences of U[32,4096] tokens, 14 q-heads / 2 kv-heads x 64, "
-                                      "block 16, shuffled frames", "kernel": "paged_decode_kernel_mma_r128<64,8,2> "
-                                      "(7 rows per kv-head on tensor cores)", "ms": round(gqa_ms, 5), "bytes": gqa_bytes,
-                          "gbs": round(gqa_bytes / (gqa_ms / 1e3) / 1e9, 1),
-                          "frac_of_measured_copy": round(gqa_bytes / (gqa_ms / 1e3) / 1e9 / peak, 4)},
-        "gqa_block_sizes": gqa_sweep,
-        "split_13b": {"workload": "40 heads x 128, 2048 tokens per sequence, block 16, shuffled frames",
-                      "rows": split13},
-        "decode_loop_gpt2": gpt2,
-        "gather": {"gbs": round(g_bytes / (gather_ms / 1e3) / 1e9, 1), "ms": round(gather_ms, 5),
-                   "bytes": g_bytes, "frac_of_measured_copy": round(g_bytes / (gather_ms / 1e3) / 1e9 / peak, 4)},
+        **side,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profile_traffic(),
-                     "kernel": "pf_decode_step (paged_decode_kernel_r128<64,1,4>: fused write, attention, in-kernel merge)",
+                     "kernel": "pf_decode_step (paged_decode_kernel_mma_r128<64,4,4>: tensor-core consumers, fused write, "
+                               "attention, in-kernel merge)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},
         "e2e": e2e,

@@ -240,10 +240,10 @@ PF_API int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stre
  * or PF_F32); n_q_heads must be a multiple of Hkv (grouped heads share one
  * page load): 1 to 8 q-heads per kv-head under any split setting, up to 16
  * with split_tokens = 0 on pages of at least 16 tokens (PF_ERR_UNSUPPORTED
- * otherwise).  With split_tokens = 0 and such pages, kv-heads of 3 or more
- * q-heads at head_dim 64 (2 or more at 128) compute the scores and the
- * weighted sum on tensor cores with the weights rounded to fp16 (within the
- * same tolerance of the exact result).  Sequences longer than split_tokens are cut into chunks whose
+ * otherwise).  With split_tokens = 0 and such pages the scores and the
+ * weighted sum are computed on tensor cores with the weights rounded to fp16
+ * (within the same tolerance of the exact result); fixed chunks and 1-token
+ * pages keep fp32 weights.  Sequences longer than split_tokens are cut into chunks whose
  * partial results are combined with the log-sum-exp rule (same section:
  * reduction across thread blocks); split_tokens 0 = choose automatically,
  * -1 = never split, > 0 = chunk length (rounded up to a multiple of 16).

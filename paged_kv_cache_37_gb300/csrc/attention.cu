@@ -25,15 +25,17 @@ LaunchShape g_shapes[kMaxDevices][2][17][5][2];
 
 // Kv-heads with at least this many rows (q-heads, or query tokens x
 // q-heads) take the tensor-core consumers when the call runs the span
-// schedule over pages of at least TB tokens.  Measured (256 sequences of
-// U[32, 4096] tokens, GB/s, tensor-core vs CUDA-core consumers): head_dim 64,
-// 2 rows 3013 vs 4088, 3 rows 2988 vs 2402, 4 rows 2976 vs 2462, 8 rows 2404
-// vs 1132; head_dim 128, 2 rows 3905 vs 2585, 8 rows 3573 vs 867.
+// schedule over pages of at least TB tokens (the CUDA-core consumers serve
+// fixed chunks and 1-token pages).  Measured (256 sequences of U[32, 4096]
+// tokens, GB/s, CUDA-core vs tensor-core consumers with their heads per
+// item): head_dim 64, 1 row 5593 vs 6358, 2 rows 4105 vs 6111, 3 rows 2402
+// vs 6044, 8 rows 1132 vs 3324; head_dim 128, 1 row 4180 vs 6123, 8 rows 867
+// vs 5248.
 #ifndef PKV_MMA_MIN_ROWS_D64
-#define PKV_MMA_MIN_ROWS_D64 3
+#define PKV_MMA_MIN_ROWS_D64 1
 #endif
 #ifndef PKV_MMA_MIN_ROWS_D128
-#define PKV_MMA_MIN_ROWS_D128 2
+#define PKV_MMA_MIN_ROWS_D128 1
 #endif
 constexpr int kMmaMaxRows = 16;
 int mma_min_rows(int head_dim) { return head_dim == 64 ? PKV_MMA_MIN_ROWS_D64 : PKV_MMA_MIN_ROWS_D128; }

@@ -28,7 +28,11 @@ def test_tiny_matches_oracle(pkv, cuda_dev, oracle_mod, split, out_f32):
     out = c.attention(scale, split=split, out_dtype=torch.float32 if out_f32 else torch.float16)
     ref = c.oracle(oracle_mod, scale)
     assert_close_to_oracle(host(out), ref, what=f"tiny split={split}")
-    if out_f32:   # fp32 output has no fp16 rounding: hold it much tighter
+    if out_f32 and split != 0:
+        # fp32 output of the CUDA-core consumers (fixed chunks) has no fp16
+        # rounding at all: hold it much tighter.  The balanced schedule's
+        # tensor-core products round the weights to fp16 and are held to the
+        # attention tolerance above.
         assert_close_to_oracle(host(out), ref, max_abs=1e-5, mean_abs=1e-6, what="tiny fp32")
     assert pkv.pf_device_status(reset=True) == 0
 
@@ -42,7 +46,10 @@ def test_tiny_brute_force_edge_lengths(pkv, cuda_dev, oracle_mod):
         out = c.attention(0.125, split=split, out_dtype=torch.float32)
         ref = c.oracle(oracle_mod, 0.125)
         assert np.all(host(out)[0] == 0.0)
-        assert_close_to_oracle(host(out), ref, max_abs=1e-5, mean_abs=1e-6, what=f"edge split={split}")
+        if split != 0:   # CUDA-core consumers: fp32 weights
+            assert_close_to_oracle(host(out), ref, max_abs=1e-5, mean_abs=1e-6, what=f"edge split={split}")
+        else:            # tensor-core consumers: fp16 weights
+            assert_close_to_oracle(host(out), ref, what=f"edge split={split}")
 
 
 def test_single_token_is_exact_value(pkv, cuda_dev):
