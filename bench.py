@@ -776,7 +776,7 @@ def run_ours(args, dist):
         **side,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profile_traffic(),
-                     "kernel": "pf_decode_step (paged_decode_kernel_mma_r128<64,4,4>: tensor-core consumers, fused write, "
+                     "kernel": "pf_decode_step (paged_decode_kernel_mma_r128<64,1,4>: tensor-core consumers, fused write, "
                                "attention, in-kernel merge)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s"},

@@ -191,8 +191,9 @@ template <int D, int G, int HG>
 struct MmaShape {
     static constexpr int STAGE_BYTES = 2 * TB * HG * D * 2;
     static constexpr int BUDGET = (D == 64 ? 228 * 1024 / 3 : 228 * 1024 / 2) - 2048;   // reserved + alignment slack
-    static constexpr int FIXED = NQ * HG * G * D * 2 + NQ * 2 * HG * D * 2 + NCW * G * (D + 2) * 4 +
-                                 (kMaxSeqsPerLaunch + 1) * 4 + kMaxSeqsPerLaunch + 2048;
+    static constexpr bool MERGE = NCW / HG > 1;   // several warps per head meet in shared memory
+    static constexpr int FIXED = NQ * HG * G * D * 2 + NQ * 2 * HG * D * 2 + (MERGE ? NCW : 1) * G * (D + 2) * 4 +
+                                 (kMaxSeqsPerLaunch + 1) * 4 + kMaxSeqsPerLaunch + 1024;   // + barriers, items
     static constexpr int NS_RAW = (BUDGET - FIXED) / STAGE_BYTES;
     static constexpr int NS = NS_RAW < 2 ? 2 : (NS_RAW > 16 ? 16 : NS_RAW);
 };
@@ -207,7 +208,7 @@ struct __align__(128) Smem {
     __half v[NS][Shape<D, HG>::STAGE_HALVES];
     __half q[NQ][HG * G * D];
     __half knew[NQ][2][HG * D];   // fused step: the new token's K and V rows of the item's heads
-    float red[(MMA || Shape<D, HG>::WPH > 1) ? NCW : 1][G][D + 2];   // per consumer warp: acc[D], m, l
+    float red[(MMA ? MmaShape<D, G, HG>::MERGE : Shape<D, HG>::WPH > 1) ? NCW : 1][G][D + 2];   // per consumer warp: acc[D], m, l
     ItemDesc desc[NQ];
     uint64_t full[NS];
     uint64_t empty[NS];
@@ -1564,7 +1565,7 @@ struct KernelInfo {
 // 1 KB of alignment slack).
 KernelInfo kernel_d64(int g, int hg);
 KernelInfo kernel_d128(int g, int hg);
-// Tensor-core instances: rows per kv-head rounded up to 4, 8 (the "_s"
+// Tensor-core instances: rows per kv-head rounded up to 1, 4, 8 (the "_s"
 // files) or 12, 16; hg 1, 2 or 4 (not 4 at head_dim 128 above 8 rows).
 KernelInfo kernel_mma_d64_s(int g, int hg);
 KernelInfo kernel_mma_d64_l(int g, int hg);
