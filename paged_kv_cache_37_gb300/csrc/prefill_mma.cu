@@ -130,29 +130,40 @@ __global__ void __launch_bounds__(NTHREADS) prefill_mma_kernel(const Params p) {
         cp_async16(smem_addr(qs + swz(row, col, QR)), ok ? src : p.q, ok ? 16u : 0u);
     }
     // Stage tile t: K and V rows of tokens t*16 .. t*16+15 up to p_max
-    // (zeros past it: never part of a result, and finite).
-    auto stage_tile = [&](int t, int stage) {
-        for (int c = threadIdx.x; c < 2 * TB * CH; c += NTHREADS) {
-            const int kv = c / (TB * CH);
-            const int rem = c - kv * (TB * CH);
-            const int row = rem / CH;
-            const int col = rem - row * CH;
+    // (zeros past it: never part of a result, and finite).  Thread x copies
+    // chunk x % CH of rows x / CH + j * (NTHREADS / CH) of K and of V, so it
+    // needs RPT block ids per tile; they are loaded LOOK tiles ahead of use
+    // (a block-table load waited for at issue would serialise the ring).
+    constexpr int RPT = TB * CH / NTHREADS;             // rows per thread and tile (1 at D = 64, 2 at 128)
+    constexpr int LOOK = 3;
+    static_assert(RPT * NTHREADS == TB * CH, "a tile's chunks split evenly over the threads");
+    const int my_col = threadIdx.x % CH;
+    const int my_row = threadIdx.x / CH;                  // rows my_row + j * (NTHREADS / CH)
+    auto load_ids = [&](int t, int (&ids)[RPT]) {
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int tok = t * TB + my_row + j * (NTHREADS / CH);
+            ids[j] = tok <= p_max ? p.bt[(size_t)s * p.max_blocks + tok / p.block_size] : 0;
+        }
+    };
+    auto stage_tile = [&](int t, int stage, const int (&ids)[RPT]) {
+#pragma unroll
+        for (int j = 0; j < RPT; ++j) {
+            const int row = my_row + j * (NTHREADS / CH);
             const int tok = t * TB + row;
-            const __half *pool = kv ? p.v_pool : p.k_pool;
-            const __half *src = pool;
-            uint32_t bytes = 0;
-            if (tok <= p_max) {
-                int id = p.bt[(size_t)s * p.max_blocks + tok / p.block_size];
-                if (id < 0 || id >= p.n_blocks) {
-                    atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
-                } else {
-                    src = pool + ((size_t)(p.layer_row0 + (long long)id * p.block_size + tok % p.block_size) *
-                                      p.n_kv_heads + h) * D + col * 8;
-                    bytes = 16;
-                }
+            int id = ids[j];
+            bool ok = tok <= p_max;
+            if (ok && (id < 0 || id >= p.n_blocks)) {
+                atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
+                ok = false;
             }
-            uint8_t *dst = (kv ? vs : ks) + stage * S::TILE_BYTES + swz(row, col, TB);
-            cp_async16(smem_addr(dst), src, bytes);
+            const size_t src =
+                ok ? ((size_t)(p.layer_row0 + (long long)id * p.block_size + tok % p.block_size) * p.n_kv_heads + h) *
+                             D + my_col * 8
+                   : 0;
+            const uint32_t off = stage * S::TILE_BYTES + swz(row, my_col, TB);
+            cp_async16(smem_addr(ks + off), p.k_pool + src, ok ? 16u : 0u);
+            cp_async16(smem_addr(vs + off), p.v_pool + src, ok ? 16u : 0u);
         }
         cp_async_commit();
     };
@@ -179,17 +190,29 @@ __global__ void __launch_bounds__(NTHREADS) prefill_mma_kernel(const Params p) {
 
     // NST - 1 tiles in flight ahead of the one being used; one commit group
     // per tile (empty past the end; q rides with tile 0), so wait_group
-    // NST - 1 means "tile t done".
+    // NST - 1 means "tile t done".  ids[k] hold the block ids of tile
+    // (next tile to stage) + k.
+    int ids[LOOK][RPT];
 #pragma unroll 1
     for (int t = 0; t < S::NST - 1; ++t) {
-        if (t < n_tiles) stage_tile(t, t);
+        int id_now[RPT];
+        load_ids(t, id_now);
+        if (t < n_tiles) stage_tile(t, t, id_now);
         else cp_async_commit();
     }
+#pragma unroll
+    for (int k = 0; k < LOOK; ++k) load_ids(S::NST - 1 + k, ids[k]);
     for (int t = 0; t < n_tiles; ++t) {
         const int stage = t % S::NST;
         const int ahead = t + S::NST - 1;
-        if (ahead < n_tiles) stage_tile(ahead, ahead % S::NST);
+        if (ahead < n_tiles) stage_tile(ahead, ahead % S::NST, ids[0]);
         else cp_async_commit();
+#pragma unroll
+        for (int k = 0; k + 1 < LOOK; ++k) {
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) ids[k][j] = ids[k + 1][j];
+        }
+        load_ids(ahead + LOOK, ids[LOOK - 1]);
         cp_async_wait<S::NST - 1>();                     // tile t has landed (this thread's part)
         __syncthreads();                                 // ... and every thread's part
         if (t == 0) {
