@@ -150,6 +150,60 @@ def test_gqa_block_size_sweep_same_tokens(pkv, cuda_dev, oracle_mod):
         assert np.array_equal(r.view(np.uint16), paged[0].view(np.uint16))
 
 
+def test_gqa_full_size_every_output(pkv, cuda_dev, oracle_mod):
+    """The grouped-heads workload at full size (256 sequences of U[32, 4096]
+    tokens, 14/2 x 64, pages of 16, shuffled frames) in the launch
+    configuration the benchmark times (balanced schedule): every output
+    against the oracle."""
+    w = si.WORKLOADS["gqa"]
+    lens = si.uniform_lengths(w["n_seqs"], w["len_lo"], w["len_hi"], seed=12)
+    c = PagedCase(pkv, cuda_dev, lens, w["n_q_heads"], w["n_kv_heads"], w["head_dim"], 16)
+    out = host(c.attention(w["scale"], split=0))
+    assert_close_to_oracle(out, c.oracle(oracle_mod, w["scale"]), what="gqa full size")
+    assert pkv.pf_device_status(reset=True) == 0
+
+
+def test_13b_like_full_batch_sampled(pkv, cuda_dev, oracle_mod):
+    """The 13B-like shape at its largest batch (64 sequences of 2048 tokens,
+    40 x 128, 2.7 GB of K/V), balanced schedule and no split.  The pool is
+    filled on the device; the pages of four sampled sequences are overwritten
+    with seeded host values, and those sequences' outputs (which read only
+    their own pages) are checked against the oracle."""
+    import torch
+    w = si.WORKLOADS["13b"]
+    S, L, H, D, B = 64, w["context_len"], w["n_q_heads"], w["head_dim"], w["block_size"]
+    pages = L // B
+    N = S * pages
+    bt = si.block_tables(np.full(S, L, dtype=np.int32), B, N, si.SEED_SHUFFLE, max_blocks=pages)
+    gen = torch.Generator(device=cuda_dev)
+    gen.manual_seed(77)
+    k = torch.randn((1, N, B, H, D), generator=gen, device=cuda_dev, dtype=torch.float32).half()
+    v = torch.randn((1, N, B, H, D), generator=gen, device=cuda_dev, dtype=torch.float32).half()
+    sample = np.array([0, 17, 40, 63])
+    kh = si.fp16_normal((len(sample), pages, B, H, D), 78)
+    vh = si.fp16_normal((len(sample), pages, B, H, D), 79)
+    for j, s in enumerate(sample):
+        ids = torch.from_numpy(bt[s].astype(np.int64)).to(cuda_dev)
+        k[0, ids] = dev(kh[j], cuda_dev)
+        v[0, ids] = dev(vh[j], cuda_dev)
+    q = si.fp16_normal((S, H, D), 80)
+    pool = pkv.pf_pool_create(k, v)
+    bt_dev, lens_dev = dev(bt, cuda_dev), dev(np.full(S, L, dtype=np.int32), cuda_dev)
+    # the oracle over the sampled sequences: contiguous K/V of each, pages in table order
+    kc = kh.reshape(len(sample), L, H, D).reshape(-1, H, D)
+    vc = vh.reshape(len(sample), L, H, D).reshape(-1, H, D)
+    off = np.arange(len(sample) + 1, dtype=np.int64) * L
+    ref = oracle_mod.attention_contiguous(q[sample], kc, vc, off, np.full(len(sample), L, dtype=np.int32), w["scale"])
+    for split in (0, -1):
+        out = torch.empty((S, H, D), dtype=torch.float16, device=cuda_dev)
+        ws = pkv.make_workspace(pool, S, H, pages, split)
+        pkv.pf_paged_decode_attention(pool, 0, dev(q, cuda_dev), bt_dev, lens_dev, w["scale"], out, split, ws)
+        torch.cuda.synchronize()
+        assert_close_to_oracle(host(out)[sample], ref, what=f"13b batch 64 split={split}")
+    assert pkv.pf_device_status(reset=True) == 0
+    del k, v
+
+
 # q-heads per kv-head from 1 to 16 at both head sizes: 4 and more take the
 # tensor-core consumers under the balanced schedule; up to 8 also run under
 # fixed chunks (CUDA-core consumers), more than 8 only under the balanced one
