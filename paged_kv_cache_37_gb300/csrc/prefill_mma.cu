@@ -20,6 +20,8 @@
 // to fp16; l sums those rounded weights.  CTAs walk their tiles in order up
 // to the last position any of their rows sees; the grid takes the q-tiles of
 // a head longest first.
+#include <type_traits>
+
 #include "device_common.cuh"
 #include "internal.h"
 
@@ -58,7 +60,7 @@ struct Params {
 
 template <int D>
 struct Shape {
-    static constexpr int NST = D == 64 ? 8 : 5;       // K/V stages
+    static constexpr int NST = D == 64 ? 9 : 6;       // K/V stages
     static constexpr int TILE_BYTES = TB * D * 2;     // K or V of one tile
     static constexpr int SMEM = QR * D * 2 + 2 * NST * TILE_BYTES;
 };
@@ -188,32 +190,122 @@ __global__ void __launch_bounds__(NTHREADS) prefill_mma_kernel(const Params p) {
     for (int b = 0; b < NNB; ++b) o[b][0] = o[b][1] = o[b][2] = o[b][3] = 0.0f;
     uint32_t qa[NKS][4];
 
-    // NST - 1 tiles in flight ahead of the one being used; one commit group
-    // per tile (empty past the end; q rides with tile 0), so wait_group
-    // NST - 1 means "tile t done".  ids[k] hold the block ids of tile
-    // (next tile to stage) + k.
-    int ids[LOOK][RPT];
+    // Tiles are used two at a time, as one 32-token softmax step.  NST - 2
+    // tiles are in flight ahead of the pair in use; one commit group per tile
+    // (empty past the end; q rides with tile 0), so wait_group NST - 2 after
+    // staging the pair's successors means "tiles t and t + 1 done".  ids[k]
+    // hold the block ids of tile (next tile to stage) + k.
+    constexpr int LOOK2 = 2 * LOOK;
+    int ids[LOOK2][RPT];
 #pragma unroll 1
-    for (int t = 0; t < S::NST - 1; ++t) {
+    for (int t = 0; t < S::NST - 2; ++t) {
         int id_now[RPT];
         load_ids(t, id_now);
         if (t < n_tiles) stage_tile(t, t, id_now);
         else cp_async_commit();
     }
 #pragma unroll
-    for (int k = 0; k < LOOK; ++k) load_ids(S::NST - 1 + k, ids[k]);
-    for (int t = 0; t < n_tiles; ++t) {
-        const int stage = t % S::NST;
-        const int ahead = t + S::NST - 1;
-        if (ahead < n_tiles) stage_tile(ahead, ahead % S::NST, ids[0]);
-        else cp_async_commit();
+    for (int k = 0; k < LOOK2; ++k) load_ids(S::NST - 2 + k, ids[k]);
+
+    // One softmax step over NT consecutive staged tiles (sub-tile u at stage
+    // (t + u) % NST, tokens tile0 + 16 u ..).
+    auto step = [&](int t, auto nt_c) {
+        constexpr int NT = decltype(nt_c)::value;
+        const int tile0 = t * TB;
+        const bool masked = tile0 + NT * TB - 1 > wlim_lo;
+        // S = Q K^T: K rows are the B fragments' columns (tokens)
+        float sc[2 * NT][4];
 #pragma unroll
-        for (int k = 0; k + 1 < LOOK; ++k) {
+        for (int u = 0; u < NT; ++u) {
+            const uint32_t kb = smem_addr(ks + ((t + u) % S::NST) * S::TILE_BYTES);
 #pragma unroll
-            for (int j = 0; j < RPT; ++j) ids[k][j] = ids[k + 1][j];
+            for (int nb = 0; nb < 2; ++nb) {
+                float *c = sc[2 * u + nb];
+                c[0] = c[1] = c[2] = c[3] = 0.0f;
+#pragma unroll
+                for (int kp = 0; kp < NKS / 2; ++kp) {
+                    uint32_t b[4];
+                    ldmatrix_x4(b, kb + swz(nb * 8 + (lane & 7), kp * 4 + (lane >> 3), TB));
+                    mma_f16_16816(sc[2 * u + nb], qa[2 * kp], b[0], b[1]);
+                    mma_f16_16816(sc[2 * u + nb], qa[2 * kp + 1], b[2], b[3]);
+                }
+            }
         }
-        load_ids(ahead + LOOK, ids[LOOK - 1]);
-        cp_async_wait<S::NST - 1>();                     // tile t has landed (this thread's part)
+#pragma unroll
+        for (int cb = 0; cb < 2 * NT; ++cb) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                sc[cb][e] *= p.scale_log2;
+                if (masked && tile0 + cb * 8 + 2 * tq + (e & 1) > lim[e >> 1]) sc[cb][e] = -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float mt = -INFINITY;
+#pragma unroll
+            for (int cb = 0; cb < 2 * NT; ++cb) mt = fmaxf(mt, fmaxf(sc[cb][2 * r], sc[cb][2 * r + 1]));
+            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
+            mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
+            if (mt > m[r] + kRescaleLog2) {
+                const float f = exp2f(m[r] - mt);         // m = -inf gives 0
+                l[r] *= f;
+#pragma unroll
+                for (int b = 0; b < NNB; ++b) {
+                    o[b][2 * r] *= f;
+                    o[b][2 * r + 1] *= f;
+                }
+                m[r] = mt;
+            }
+        }
+        // weights of sub-tile u as the A fragment of P V: register 2 nb + r
+        // holds row g + 8 r, tokens 8 nb + 2t, 8 nb + 2t + 1 of the sub-tile
+        uint32_t pa[NT][4];
+#pragma unroll
+        for (int u = 0; u < NT; ++u) {
+#pragma unroll
+            for (int nb = 0; nb < 2; ++nb) {
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const float z0 = sc[2 * u + nb][2 * r], z1 = sc[2 * u + nb][2 * r + 1];
+                    const float p0 = z0 == -INFINITY ? 0.0f : exp2f(z0 - m[r]);
+                    const float p1 = z1 == -INFINITY ? 0.0f : exp2f(z1 - m[r]);
+                    const __half2 w = __floats2half2_rn(p0, p1);
+                    const float2 wf = __half22float2(w);
+                    l[r] += wf.x + wf.y;
+                    pa[u][2 * nb + r] = *reinterpret_cast<const uint32_t *>(&w);
+                }
+            }
+        }
+        // O += P V: V rows (tokens) are the B fragments' k
+#pragma unroll
+        for (int u = 0; u < NT; ++u) {
+            const uint32_t vb = smem_addr(vs + ((t + u) % S::NST) * S::TILE_BYTES);
+#pragma unroll
+            for (int np = 0; np < NNB / 2; ++np) {
+                uint32_t b[4];
+                ldmatrix_x4_trans(b, vb + swz((lane & 7) + ((lane >> 3) & 1) * 8, np * 2 + (lane >> 4), TB));
+                mma_f16_16816(o[2 * np], pa[u], b[0], b[1]);
+                mma_f16_16816(o[2 * np + 1], pa[u], b[2], b[3]);
+            }
+        }
+    };
+
+    for (int t = 0; t < n_tiles; t += 2) {
+        // the pair's successors go into the stages of the previous pair
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int a = t + S::NST - 2 + u;
+            if (a < n_tiles) stage_tile(a, a % S::NST, ids[u]);
+            else cp_async_commit();
+        }
+#pragma unroll
+        for (int k = 0; k + 2 < LOOK2; ++k) {
+#pragma unroll
+            for (int j = 0; j < RPT; ++j) ids[k][j] = ids[k + 2][j];
+        }
+        load_ids(t + S::NST - 2 + LOOK2, ids[LOOK2 - 2]);
+        load_ids(t + S::NST - 1 + LOOK2, ids[LOOK2 - 1]);
+        cp_async_wait<S::NST - 2>();                     // tiles t, t + 1 have landed (this thread's part)
         __syncthreads();                                 // ... and every thread's part
         if (t == 0) {
             // q as A fragments: lanes 0-7 / 8-15 / 16-23 / 24-31 give rows
@@ -223,72 +315,12 @@ __global__ void __launch_bounds__(NTHREADS) prefill_mma_kernel(const Params p) {
             for (int kk = 0; kk < NKS; ++kk)
                 ldmatrix_x4(qa[kk], smem_addr(qs + swz(lrow, 2 * kk + (lane >> 4), QR)));
         }
-        const int tile0 = t * TB;
-        if (warp_rows && tile0 <= wlim_hi) {
-            const uint32_t kb = smem_addr(ks + stage * S::TILE_BYTES);
-            const uint32_t vb = smem_addr(vs + stage * S::TILE_BYTES);
-            const bool masked = tile0 + TB - 1 > wlim_lo;
-            // S = Q K^T: K rows are the B fragments' columns (tokens)
-            float sc[2][4];
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-                sc[nb][0] = sc[nb][1] = sc[nb][2] = sc[nb][3] = 0.0f;
-#pragma unroll
-                for (int kp = 0; kp < NKS / 2; ++kp) {
-                    uint32_t b[4];
-                    ldmatrix_x4(b, kb + swz(nb * 8 + (lane & 7), kp * 4 + (lane >> 3), TB));
-                    mma_f16_16816(sc[nb], qa[2 * kp], b[0], b[1]);
-                    mma_f16_16816(sc[nb], qa[2 * kp + 1], b[2], b[3]);
-                }
-            }
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    sc[nb][e] *= p.scale_log2;
-                    if (masked && tile0 + nb * 8 + 2 * tq + (e & 1) > lim[e >> 1]) sc[nb][e] = -INFINITY;
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                float mt = fmaxf(fmaxf(sc[0][2 * r], sc[0][2 * r + 1]), fmaxf(sc[1][2 * r], sc[1][2 * r + 1]));
-                mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 1));
-                mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 2));
-                if (mt > m[r] + kRescaleLog2) {
-                    const float f = exp2f(m[r] - mt);     // m = -inf gives 0
-                    l[r] *= f;
-#pragma unroll
-                    for (int b = 0; b < NNB; ++b) {
-                        o[b][2 * r] *= f;
-                        o[b][2 * r + 1] *= f;
-                    }
-                    m[r] = mt;
-                }
-            }
-            uint32_t pa[4];
-#pragma unroll
-            for (int nb = 0; nb < 2; ++nb) {
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
-                    const float z0 = sc[nb][2 * r], z1 = sc[nb][2 * r + 1];
-                    const float p0 = z0 == -INFINITY ? 0.0f : exp2f(z0 - m[r]);
-                    const float p1 = z1 == -INFINITY ? 0.0f : exp2f(z1 - m[r]);
-                    const __half2 w = __floats2half2_rn(p0, p1);
-                    const float2 wf = __half22float2(w);
-                    l[r] += wf.x + wf.y;
-                    pa[2 * nb + r] = *reinterpret_cast<const uint32_t *>(&w);
-                }
-            }
-            // O += P V: V rows (tokens) are the B fragments' k
-#pragma unroll
-            for (int np = 0; np < NNB / 2; ++np) {
-                uint32_t b[4];
-                ldmatrix_x4_trans(b, vb + swz((lane & 7) + ((lane >> 3) & 1) * 8, np * 2 + (lane >> 4), TB));
-                mma_f16_16816(o[2 * np], pa, b[0], b[1]);
-                mma_f16_16816(o[2 * np + 1], pa, b[2], b[3]);
-            }
+        if (warp_rows && t * TB <= wlim_hi) {
+            // a pair, or the last tile alone (its partner was never staged)
+            if (t + 1 < n_tiles && (t + 1) * TB <= wlim_hi) step(t, std::integral_constant<int, 2>());
+            else step(t, std::integral_constant<int, 1>());
         }
-        __syncthreads();                                 // the stage is refilled NST - 1 tiles later
+        __syncthreads();                                 // the pair's stages are refilled next iteration
     }
     cp_async_wait<0>();
 
