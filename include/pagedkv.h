@@ -308,11 +308,14 @@ PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
  * initialised once with pf_decode_workspace_init, not shared by overlapping
  * calls) and max_new_tokens x (n_q_heads / Hkv) <= 8 (16 on pages of at
  * least 16 tokens), the decode kernel serves the new tokens as extra rows of
- * each kv-head -- balanced spans over
- * the contexts, every K/V byte read once per kv-head (a chunked append);
- * otherwise (workspace null, or longer appends and prompts) a kernel that
- * needs no workspace walks each (chunk of new tokens, kv-head) over its
- * context. */
+ * each kv-head -- balanced spans over the contexts, every K/V byte read once
+ * per kv-head (a chunked append); otherwise (workspace null, or longer
+ * appends and prompts) a kernel that needs no workspace takes 64 query rows
+ * (new tokens x q-heads) of one (sequence, kv-head) per block and walks the
+ * context up to their last position.  Both compute the products on tensor
+ * cores with the softmax weights rounded to fp16 (within the attention
+ * tolerance), except the decode kernel on 1-token pages (fp32 weights).
+ * Up to 16 q-heads per kv-head. */
 PF_API int pf_paged_prefill_attention(const pf_pool *pool, int layer,
                                       const void *q,
                                       const int32_t *block_tables,
