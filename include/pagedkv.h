@@ -242,8 +242,8 @@ PF_API int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stre
  * with split_tokens = 0 on pages of at least 16 tokens (PF_ERR_UNSUPPORTED
  * otherwise).  With split_tokens = 0 and such pages the scores and the
  * weighted sum are computed on tensor cores with the weights rounded to fp16
- * (within the same tolerance of the exact result); fixed chunks and 1-token
- * pages keep fp32 weights.  Sequences longer than split_tokens are cut into chunks whose
+ * (within the same tolerance of the exact result); fixed chunks keep fp32
+ * weights.  Sequences longer than split_tokens are cut into chunks whose
  * partial results are combined with the log-sum-exp rule (same section:
  * reduction across thread blocks); split_tokens 0 = choose automatically,
  * -1 = never split, > 0 = chunk length (rounded up to a multiple of 16).
@@ -314,7 +314,7 @@ PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
  * (new tokens x q-heads) of one (sequence, kv-head) per block and walks the
  * context up to their last position.  Both compute the products on tensor
  * cores with the softmax weights rounded to fp16 (within the attention
- * tolerance), except the decode kernel on 1-token pages (fp32 weights).
+ * tolerance).
  * Up to 16 q-heads per kv-head. */
 PF_API int pf_paged_prefill_attention(const pf_pool *pool, int layer,
                                       const void *q,

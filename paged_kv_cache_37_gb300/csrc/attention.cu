@@ -25,8 +25,7 @@ LaunchShape g_shapes[kMaxDevices][2][17][5][2];
 
 // Kv-heads with at least this many rows (q-heads, or query tokens x
 // q-heads) take the tensor-core consumers when the call runs the span
-// schedule over pages of at least TB tokens (the CUDA-core consumers serve
-// fixed chunks and 1-token pages).  Measured (256 sequences of U[32, 4096]
+// schedule (the CUDA-core consumers serve fixed chunks).  Measured (256 sequences of U[32, 4096]
 // tokens, GB/s, CUDA-core vs tensor-core consumers with their heads per
 // item): head_dim 64, 1 row 5593 vs 6358, 2 rows 4105 vs 6111, 3 rows 2402
 // vs 6044, 8 rows 1132 vs 3324; head_dim 128, 1 row 4180 vs 6123, 8 rows 867
@@ -139,7 +138,7 @@ namespace {
 // kv-head per item, its tensor map the swizzled one).
 int kernel_for(const pf_pool *pool, int n_q_heads, bool spans, KernelInfo *ki, int *hg, bool *mma) {
     const int G = n_q_heads / pool->n_kv_heads;
-    *mma = spans && pool->block_size >= TB && G >= mma_min_rows(pool->head_dim) && G <= kMmaMaxRows;
+    *mma = spans && G >= mma_min_rows(pool->head_dim) && G <= kMmaMaxRows;
     if (*mma) {
         *hg = mma_heads(pool->n_kv_heads, G, pool->head_dim);
         *ki = kernel_mma(pool->head_dim, G, *hg);

@@ -266,6 +266,14 @@ struct ProdItem {
     int qrow0, nq;    // q row of the sequence's first query token; its query tokens
 };
 
+// Byte offset, in an MMA stage (one kv-head), of 16-byte chunk c (dims
+// 8c .. 8c + 7) of tile row t: per 64-dim half, TB rows of 128 bytes, chunk
+// c % 8 of row t stored at position (c % 8) ^ (t % 8) -- the layout a TMA
+// copy with 128-byte swizzling writes at a 1024-byte aligned stage.
+__device__ __forceinline__ uint32_t swz(int t, int c) {
+    return (uint32_t)((((c >> 3) * TB + t) << 7) + ((((c & 7) ^ (t & 7))) << 4));
+}
+
 // Issue one K or V tile (pool rows r .. r + TB - 1 of heads h0 ..) into a
 // stage.  Plain: one box {D, HG, TB}.  MMA: per head and 64-element half of
 // the head, one swizzled box {64, TB} to stage offset (head * D / 64 + half)
@@ -589,6 +597,29 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
                     tma_load_3d(smem_addr(sm.k[stage] + off), tmk, 0, it.h0, r, full_bar, pol);
                     tma_load_3d(smem_addr(sm.v[stage] + off), tmv, 0, it.h0, r, full_bar, pol);
                 }
+            } else {
+                // B < TB (B = 1) in the tensor-core layout: each token row
+                // goes by cp.async to its swizzled place (a TMA box of one
+                // row could not follow the swizzle).  Lanes 0-15 copy K and
+                // 16-31 V of token lane % 16; every lane's copies complete on
+                // the stage's full barrier (32 arrivals for these stages).
+                const int tk = lane & 15;
+                const int raw = __shfl_sync(FULL, cur, (pa - wbase + tk) & 31);   // page of token t + tk
+                if (tk < nt) {
+                    const int id = checked(raw);
+                    const size_t row = (size_t)(p.layer_row0 + id * B + (t + tk) % B);
+                    const __half *src = (lane < 16 ? p.k_pool : p.v_pool) + (row * p.n_kv_heads + it.h0) * D;
+                    uint8_t *dst = reinterpret_cast<uint8_t *>(lane < 16 ? sm.k[stage] : sm.v[stage]);
+#pragma unroll
+                    for (int hl = 0; hl < HG; ++hl) {
+                        if (it.h0 + hl < p.n_kv_heads) {
+#pragma unroll
+                            for (int c = 0; c < D / 8; ++c)
+                                cp_async16_cg(smem_addr(dst + hl * (D / 64) * TB * 128 + swz(tk, c)), src + hl * D + c * 8);
+                        }
+                    }
+                }
+                cp_async_mbar_arrive_noinc(full_bar);
             }
         }
         if (!ok) break;
@@ -1102,14 +1133,6 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
 
 // ------------------------------------------------------------ tensor-core consumers
 
-// Byte offset, in an MMA stage (one kv-head), of 16-byte chunk c (dims
-// 8c .. 8c + 7) of tile row t: per 64-dim half, TB rows of 128 bytes, chunk
-// c % 8 of row t stored at position (c % 8) ^ (t % 8) -- the layout a TMA
-// copy with 128-byte swizzling writes at a 1024-byte aligned stage.
-__device__ __forceinline__ uint32_t swz(int t, int c) {
-    return (uint32_t)((((c >> 3) * TB + t) << 7) + ((((c & 7) ^ (t & 7))) << 4));
-}
-
 // Two consecutive output values of one row.
 __device__ __forceinline__ void store2(const Params &p, size_t o, float x0, float x1) {
     if (p.out_f32) *reinterpret_cast<float2 *>(static_cast<float *>(p.out) + o) = make_float2(x0, x1);
@@ -1431,7 +1454,10 @@ __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const C
     prefetch_table_rows(p);
     if (threadIdx.x == 0) {
         for (int i = 0; i < NS; ++i) {
-            mbar_init(smem_addr(&sm.full[i]), 1);
+            // tensor-core layout on pages of fewer than TB tokens: the
+            // producer's 32 lanes arrive (cp.async); otherwise one arrival
+            // with the TMA byte count
+            mbar_init(smem_addr(&sm.full[i]), (MMA && p.block_size < TB) ? 32 : 1);
             mbar_init(smem_addr(&sm.empty[i]), NCW);
         }
         for (int i = 0; i < NQ; ++i) {

@@ -173,6 +173,18 @@ __device__ __forceinline__ void fence_proxy_async_shared() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 16-byte cp.async (L2 only) from global to shared memory.
+__device__ __forceinline__ void cp_async16_cg(uint32_t smem, const void *gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem), "l"(gmem) : "memory");
+}
+
+// The mbarrier counts one arrival when every cp.async this thread issued so
+// far has completed (.noinc: the arrival counts toward the barrier's expected
+// count, which must include it).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Four 8x8 b16 matrices from shared memory: lanes 8i .. 8i + 7 give the row
 // addresses (16 bytes each) of matrix i; register i receives matrix i, lane l
 // holding row l / 4, columns 2 (l % 4) and 2 (l % 4) + 1.  With .trans, lane l
