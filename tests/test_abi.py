@@ -87,6 +87,14 @@ def test_device_calls_reject_bad_arguments_before_launch(pkv):
     assert lib.pf_paged_decode_attention(*args(hq=12 * 9, split=64)) == pkv.PF_ERR_UNSUPPORTED
     assert lib.pf_decode_workspace_bytes(pool, 4, 12 * 16, 7, 0) > 0    # 16 rows: balanced schedule only
     assert lib.pf_decode_workspace_bytes(pool, 4, 12 * 16, 7, -1) == 0
+    # balanced schedule: records hold the rows of the tensor-core instance
+    # (rows rounded up to 1, 4, 8, 12, 16), so sizes step with the instance
+    ws = {g: lib.pf_decode_workspace_bytes(pool, 4, 12 * g, 7, 0) for g in range(1, 17)}
+    assert ws[2] == ws[3] == ws[4] and ws[5] == ws[8] and ws[9] == ws[12] and ws[13] == ws[16]
+    assert ws[1] < ws[4] < ws[8] < ws[12] < ws[16]
+    # fixed chunks: CUDA-core instances, records of exactly G rows
+    wc = {g: lib.pf_decode_workspace_bytes(pool, 4, 12 * g, 7, 16) for g in range(1, 9)}
+    assert all(wc[g] < wc[g + 1] for g in range(1, 8))
     assert lib.pf_paged_decode_attention(*args(dt=3)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_decode_attention(*args(scale=0.0)) == pkv.PF_ERR_INVALID
     assert lib.pf_paged_decode_attention(*args(scale=float("nan"))) == pkv.PF_ERR_INVALID
