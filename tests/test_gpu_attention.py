@@ -148,6 +148,34 @@ def test_gqa_block_size_sweep_same_tokens(pkv, cuda_dev, oracle_mod):
         assert np.array_equal(r.view(np.uint16), results[0].view(np.uint16))
 
 
+@pytest.mark.parametrize("hq,hkv", [(8, 2), (4, 4)])
+def test_one_token_pages_head_dim_128(pkv, cuda_dev, oracle_mod, hq, hkv):
+    """head_dim 128 on 1-token pages (rows staged by cp.async into the
+    two-half tile layout): the oracle's result, and bit-identical to the same
+    tokens on 16-token pages."""
+    lens = si.uniform_lengths(9, 1, 300, seed=31)
+    D = 128
+    off = si.cu_offsets(lens)
+    T = int(off[-1])
+    kc = si.fp16_normal((T, hkv, D), 311)
+    vc = si.fp16_normal((T, hkv, D), 312)
+    q = si.fp16_normal((len(lens), hq, D), 313)
+    scale = float(np.float32(1.0 / math.sqrt(D)))
+    ref = oracle_mod.attention_contiguous(q, kc, vc, off, lens, scale)
+    seq_idx = np.repeat(np.arange(len(lens)), lens).astype(np.int32)
+    pos = np.concatenate([np.arange(L) for L in lens]).astype(np.int32)
+    outs = []
+    for B in (1, 16):
+        c = PagedCase(pkv, cuda_dev, lens, hq, hkv, D, B)
+        pkv.pf_write_kv(c.pool, 0, dev(kc, cuda_dev), dev(vc, cuda_dev), c.bt_dev,
+                        dev(seq_idx, cuda_dev), dev(pos, cuda_dev))
+        out = host(c.attention(scale, q_dev=dev(q, cuda_dev)))
+        assert_close_to_oracle(out, ref, what=f"{hq}/{hkv}x128 B={B}")
+        outs.append(out)
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    assert pkv.pf_device_status(reset=True) == 0
+
+
 def test_gqa_full_size_every_output(pkv, cuda_dev, oracle_mod):
     """The grouped-heads workload at full size (256 sequences of U[32, 4096]
     tokens, 14/2 x 64, pages of 16, shuffled frames) in the launch
