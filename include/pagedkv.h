@@ -8,8 +8,11 @@
  *   failure pf_last_error() gives a message (per calling thread) and nothing
  *   was launched or changed.
  * - Device pointers are owned by the caller (e.g. PyTorch tensors); the
- *   library never allocates or frees device memory.  Host handles
- *   (pf_pool, pf_alloc) are allocated by *_create and released by *_destroy.
+ *   library makes no device allocation and frees none.  Its only device
+ *   memory is static, per device, for the life of the process: a status
+ *   word (pf_device_status) and the fixed 8 MiB scratch of
+ *   pf_paged_decode_attention_noalloc.  Host handles (pf_pool, pf_alloc)
+ *   are allocated by *_create and released by *_destroy.
  * - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *   stream).  Device calls are asynchronous on that stream; the caller keeps
  *   the buffers alive until the work completes.
@@ -222,12 +225,12 @@ PF_API size_t pf_decode_workspace_bytes(const pf_pool *pool, int n_seqs,
                                  int split_tokens);
 
 /* Prepare a workspace for first use (zero it).  Needed once after the
- * workspace is allocated: merge jobs in the workspace are recognised by a
- * per-call stamp (zeroed memory holds no stamp of any call), and the
- * counters that tell which block merges a split sequence must start at zero.
- * Every call that completes leaves the workspace ready for the next one.
- * After a call that set PF_DEV_WAIT_TIMEOUT, initialise the workspace again
- * before reusing it. */
+ * workspace is allocated: everything a call reads back from the workspace
+ * (merge jobs, the partial records of split sequences) carries a stamp of
+ * the launch that wrote it, and zeroed memory holds no stamp of any launch.
+ * Nothing else needs resetting, so every call -- one that set
+ * PF_DEV_WAIT_TIMEOUT included -- leaves the workspace ready for the next.
+ * Stamps count launches in the process (2^32 of them before they repeat). */
 PF_API int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 
 /* Single-query decode attention through the block tables (PagedAttention
@@ -349,11 +352,14 @@ PF_API size_t pf_prefill_workspace_bytes(const pf_pool *pool, int n_seqs,
  * - The first call on a device looks up the array's device address (once
  *   per device, with that device current); make that first call before any
  *   stream capture.
- * - Every call on a device uses the same array.  A call that completes
- *   leaves it ready for the next one; after a call that set
- *   PF_DEV_WAIT_TIMEOUT, pf_device_status with reset != 0 zeroes it again.
- *   Calls that overlap on the GPU (other streams, other threads) race on
- *   the scratch: order them on one stream. */
+ * - Every call on a device uses the same array, and each call leaves it
+ *   ready for the next one (a call that set PF_DEV_WAIT_TIMEOUT included:
+ *   what a call reads back carries its own launch's stamp).  Calls that
+ *   overlap on the GPU (other streams, other threads) race on the scratch:
+ *   order them on one stream.
+ * - The device address is kept for the life of the process; after
+ *   cudaDeviceReset (or anything else that tears down the device's primary
+ *   context) this call must not be used again in that process. */
 PF_API int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
                                              const void *q,
                                              const int32_t *block_tables,
@@ -366,9 +372,7 @@ PF_API int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
 
 /* Read the device status word (OR of pf_device_flag bits set by kernels of
  * this library on the current device since the last reset) into *status_out.
- * Synchronises `stream`.  reset != 0 clears the word afterwards and, when the
- * word held PF_DEV_WAIT_TIMEOUT, zeroes the scratch of
- * pf_paged_decode_attention_noalloc on this device. */
+ * Synchronises `stream`.  reset != 0 clears the word afterwards. */
 PF_API int pf_device_status(int *status_out, int reset, void *stream);
 
 #ifdef __cplusplus

@@ -393,12 +393,6 @@ int pf_device_status(int *status_out, int reset, void *stream) {
         e = cudaMemsetAsync(dev, 0, sizeof(int), s);
         if (e == cudaSuccess) e = cudaStreamSynchronize(s);
         if (e != cudaSuccess) return pkv::cuda_error(e, "pf_device_status: reset");
-        // A call that gave up waiting may have left arrival counters behind
-        // in the built-in scratch, which its callers cannot re-initialize.
-        if (host & PF_DEV_WAIT_TIMEOUT) {
-            const int rc = pkv::noalloc_scratch_reset(s);
-            if (rc) return rc;
-        }
     }
     return PF_OK;
 }

@@ -212,16 +212,17 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
     plan->spans = split_tokens == 0;
     int rc = kernel_for(pool, n_q_heads, plan->spans, &ki, &HG, &mma);
     if (rc) return rc;
-    const size_t rec_bytes = (size_t)ki.rows * (size_t)(pool->head_dim + 2) * sizeof(float);
+    // a record: the rows of the kernel instance x (D + 2) words (acc, m, l);
+    // fp32 for fixed chunks, 64-bit (value, epoch) for spans
+    const size_t rec_words = (size_t)ki.rows * (size_t)(pool->head_dim + 2);
     const int per_launch = n_seqs < attn::kMaxSeqsPerLaunch ? n_seqs : attn::kMaxSeqsPerLaunch;
     plan->grid = 0;
     if (need_device) {
         rc = resident_grid(pool, n_q_heads, plan->spans, &plan->grid);
         if (rc) return rc;
     }
-    // [reserved: 256 B][fp32 records][arrival counters][merge jobs]
+    // [reserved: 256 B][records][merge jobs]
     plan->counter_bytes = 256;
-    plan->arrival_bytes = 0;
     const int ng = (pool->n_kv_heads + HG - 1) / HG;
     if (plan->spans) {
         plan->chunk = TB;
@@ -231,13 +232,11 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
             grid = kGridBoundNoDevice;
         }
         // two records (first and last segment of a span) per span and head
-        // of the group; one arrival counter per span and head (a span is the
-        // first span of at most one cut pair).  Cut pairs are merged inside
-        // the kernel, so there are no jobs.
+        // of the group.  Cut pairs are merged inside the kernel, so there
+        // are no jobs.
         const size_t spans = (size_t)grid;
         plan->n_jobs = 0;
-        plan->arrival_bytes = spans * (size_t)HG * sizeof(unsigned);
-        plan->partial_bytes = spans * 2 * (size_t)HG * rec_bytes + plan->arrival_bytes;
+        plan->partial_bytes = spans * 2 * (size_t)HG * rec_words * sizeof(unsigned long long);
     } else {
         long long c = split_tokens == -1 ? cap : ((long long)split_tokens + TB - 1) / TB * TB;
         if (c > cap) c = cap;
@@ -250,7 +249,8 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
         } else {
             const size_t units = (size_t)per_launch * (size_t)per_seq;
             plan->n_jobs = units * ng;
-            plan->partial_bytes = units * (size_t)pool->n_kv_heads * rec_bytes + plan->n_jobs * sizeof(attn::Job);
+            plan->partial_bytes =
+                units * (size_t)pool->n_kv_heads * rec_words * sizeof(float) + plan->n_jobs * sizeof(attn::Job);
         }
     }
     return PF_OK;
@@ -278,10 +278,10 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     p.k_pool = static_cast<__half *>(pool->k_base);
     p.v_pool = static_cast<__half *>(pool->v_base);
     uint8_t *ws = static_cast<uint8_t *>(a.workspace);
-    const size_t rec_bytes = plan.partial_bytes - plan.arrival_bytes - plan.n_jobs * sizeof(attn::Job);
+    const size_t rec_bytes = plan.partial_bytes - plan.n_jobs * sizeof(attn::Job);
     p.partials = reinterpret_cast<float *>(ws + plan.counter_bytes);
-    p.arrivals = reinterpret_cast<unsigned *>(ws + plan.counter_bytes + rec_bytes);
-    p.jobs = reinterpret_cast<attn::Job *>(ws + plan.counter_bytes + rec_bytes + plan.arrival_bytes);
+    p.span_recs = reinterpret_cast<unsigned long long *>(ws + plan.counter_bytes);
+    p.jobs = reinterpret_cast<attn::Job *>(ws + plan.counter_bytes + rec_bytes);
     p.status = status;
     p.max_blocks = a.max_blocks;
     p.n_q_heads = a.n_q_heads;
@@ -294,13 +294,14 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     p.spans = plan.spans ? 1 : 0;
     p.out_f32 = a.out_dtype == PF_F32;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    // L2 prefetch before the dependency wait: a ring's worth when nothing
-    // overlaps (the loads follow at once), deeper when the launch overlaps the
-    // previous kernel's tail.  Measured on the mixed workload, back to back:
-    // 4 tiles 42.75 us, 8: 41.9, 16: 41.5, 20: 42.0, 24: 43.3 (per CTA x 456
-    // CTAs, 16 tiles is about the size of L2); called alone, 16 tiles cost
-    // 2 us more than 4.
-    p.prefetch_tiles = a.overlap_previous ? 16 : 4;
+    // L2 prefetch of each CTA's first tiles before the dependency wait.
+    // Measured on the mixed workload: back to back (the launch overlaps the
+    // previous kernel's tail), 4 tiles 42.75 us, 8: 41.9, 16: 41.5, 20: 42.0,
+    // 24: 43.3 (16 tiles per CTA x 456 CTAs is about the size of L2); a call
+    // on its own, 0 tiles 42.0-42.9 us, 2: 41.9-42.0, 4: 41.4-41.6, 6:
+    // 41.2, 8: 41.3-41.5, 12: 42.8.  The prefetches reach DRAM ahead of the
+    // ring's loads, which then find their lines on the way in.
+    p.prefetch_tiles = a.overlap_previous ? 16 : 6;
     p.gh = a.n_q_heads / pool->n_kv_heads;
     p.rows = a.rows;
     const size_t out_elem = a.out_dtype == PF_F32 ? 4 : 2;

@@ -44,16 +44,19 @@
 //   slot in the launch, so nothing waits for the write.
 // * End of item: token groups merge by shuffles (and the WPH warps of a head
 //   through shared memory).  A whole pair writes `out`.  A part of a cut pair
-//   writes its record (acc[D], m, l per q-head) with plain stores.
-//   - Span schedule: when its CTA has no items left, the part's warp counts
-//     it in the pair's arrival counter (one per pair and head; a GPU-scope
-//     fence, then a wrapping increment).  The part that draws the last count
-//     merges all of the pair's records with the log-sum-exp rule and writes
-//     `out`.  The wrap leaves every counter at zero for the next call.
+//   writes its record (acc[D], m, l per q-head).
+//   - Span schedule: every word of the record carries the launch's epoch
+//     (one indivisible 64-bit store per value, no fence).  The pair's last
+//     span merges it: when its CTA has no items left, the head's warp loads
+//     the pair's records, polls until every word carries this launch's
+//     epoch (the other parts belong to earlier spans, whose CTAs never wait
+//     for anyone), combines them with the log-sum-exp rule and writes
+//     `out`.  Nothing needs resetting between calls.
 //   - Chunk schedule: chunk 0 of the pair also writes a merge job stamped
 //     with the call's epoch; merge_kernel, launched next on the stream as a
 //     programmatic dependent of this grid, merges every job of this epoch.
-//   No CTA waits for another.
+//   Only a merging warp waits for other CTAs, and only for parts that need
+//   nothing from it.
 // * Every wait is bounded (1 s) and parks the thread in hardware while it
 //   waits; a timeout sets PF_DEV_WAIT_TIMEOUT and the CTA returns after
 //   waiting (bounded) for its own copies in flight.
@@ -128,10 +131,12 @@ struct Params {
     void *out;
     const int32_t *bt;
     const int32_t *lens;
-    float *partials;
+    float *partials;         // chunk schedule: fp32 records of the chunks of cut pairs
     struct Job *jobs;        // chunk schedule: merge jobs for merge_kernel
-    unsigned *arrivals;      // span schedule: parts of each cut pair done, per (first span, head)
-    unsigned epoch;   // this launch's stamp for merge jobs (never 0)
+    // span schedule: records of the parts of cut pairs, 64-bit words
+    // (value, epoch) per float (see st_tagged)
+    unsigned long long *span_recs;
+    unsigned epoch;   // this launch's stamp for merge jobs and span records (never 0)
     int *status;
     int n_seqs;
     int max_blocks;
@@ -165,11 +170,18 @@ struct Params {
 struct SpanMap {
     long long W;   // tiles in all
     long long n;   // spans
-    __device__ __forceinline__ SpanMap(long long W_, int grid) : W(W_), n(W_ < grid ? W_ : grid) {}
+    bool narrow;   // W * n < 2^32: the products and quotients fit 32-bit unsigned arithmetic
+    __device__ __forceinline__ SpanMap(long long W_, int grid)
+        : W(W_), n(W_ < grid ? W_ : grid), narrow(W_ * (W_ < grid ? W_ : grid) < (1ll << 32)) {}
     // first tile of span j (W for j = n)
-    __device__ __forceinline__ long long start(long long j) const { return j >= n ? W : W * j / n; }
+    __device__ __forceinline__ long long start(long long j) const {
+        if (j >= n) return W;
+        return narrow ? (long long)((unsigned)W * (unsigned)j / (unsigned)n) : W * j / n;
+    }
     // the span that holds tile x
-    __device__ __forceinline__ long long owner(long long x) const { return ((x + 1) * n - 1) / W; }
+    __device__ __forceinline__ long long owner(long long x) const {
+        return narrow ? (long long)((((unsigned)x + 1u) * (unsigned)n - 1u) / (unsigned)W) : ((x + 1) * n - 1) / W;
+    }
 };
 
 template <int D, int HG>
@@ -223,6 +235,7 @@ struct __align__(128) Smem {
     // its clamped length is (pre[s + 1] - pre[s] - kPairCost - 1) * 16 + rem[s]
     int pre[kMaxSeqsPerLaunch + 1];
     uint8_t rem[kMaxSeqsPerLaunch];
+    int s_first;   // span schedule: the sequence that holds this CTA's first unit
 };
 
 // L2 prefetch of the first min(row, max(128, kTablePrefetchBytes / S)) bytes
@@ -432,8 +445,10 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         for (;;) {
             it.done = x >= xend;
             if (it.done) return it;
-            // largest s with pre[s] * ng <= x (it has units: pre[s + 1] * ng > x)
+            // largest s with pre[s] * ng <= x (it has units: pre[s + 1] * ng > x);
+            // the prologue found it for the span's first unit
             int lo = 0, hi = S - 1;
+            if (x == sstart) lo = hi = sm.s_first;
             while (lo < hi) {
                 const int mid = (lo + hi + 1) >> 1;
                 if ((long long)sm.pre[mid] * ng <= x) lo = mid;
@@ -443,7 +458,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
             const int u = sm.pre[s + 1] - sm.pre[s];          // units of each of its pairs
             const int nt = u - kPairCost;                     // tiles of each of its pairs
             const long long pair0 = (long long)sm.pre[s] * ng;
-            const int grp = (int)((x - pair0) / u);
+            const int grp = map.narrow ? (int)((unsigned)(x - pair0) / (unsigned)u) : (int)((x - pair0) / u);
             const long long a = pair0 + (long long)grp * u;    // the pair's first unit (its cost unit)
             const int off = (int)(x - a);
             const int len = (int)min((long long)(u - off), xend - x);
@@ -492,7 +507,77 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     // Launched as a programmatic dependent: wait for the previous kernel on
     // the stream before the first read of q or the pool (a no-op otherwise).
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    for (int k = 0;; ++k) {
+
+    // Block ids of the current item: pages wbase .. wbase + 31 (lane l holds
+    // page wbase + l in cur) and the next 32 (nxt), item-relative.
+    int wbase = 0;
+    int cur = it.ids0;
+    int nxt = it.ids1;
+    // Issue tile j of the current item into the next stage (st); false when
+    // the wait for the stage gave up.
+    auto issue_tile = [&](int j) -> bool {
+        const int t = it.tok0 + j * TB;
+        const int nt = min(TB, it.tok0 + it.ntok - t);
+        const int pa = t / B - it.pg0;            // first page of the tile, item-relative
+        if (pa - wbase >= 32) {                    // move to the prefetched window
+            wbase += 32;
+            cur = nxt;
+            nxt = load_id(it.s, it.pg0, it.npg, wbase + 32);
+        }
+        const int stage = st % NS;
+        if (!warp_wait(smem_addr(&sm.empty[stage]), ((st / NS) & 1) ^ 1, p.status, lane)) return false;
+        const uint32_t full_bar = smem_addr(&sm.full[stage]);
+        if (B >= TB) {
+            // the tile is rows [t % B, t % B + TB) of one page
+            const int id = checked(__shfl_sync(FULL, cur, pa - wbase));
+            if (lane == 0) {
+                mbar_arrive_expect_tx(full_bar, kTileBytes);
+                const int r = p.layer_row0 + id * B + (t % B);
+                tile_load<D, HG, MMA>(sm.k[stage], tmk, it.h0, r, full_bar, pol);
+                tile_load<D, HG, MMA>(sm.v[stage], tmv, it.h0, r, full_bar, pol);
+            }
+        } else if constexpr (!MMA) {
+            // B < TB (B = 1): one box of B rows per page
+            const int pb = (t + nt - 1) / B - it.pg0;
+            const int np = pb - pa + 1;
+            const int raw = __shfl_sync(FULL, cur, (pa - wbase + lane) & 31);
+            if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)np * B * HG * D * 2 * 2);
+            __syncwarp();
+            if (lane < np) {
+                const int r = p.layer_row0 + checked(raw) * B;
+                const int off = lane * B * HG * D;
+                tma_load_3d(smem_addr(sm.k[stage] + off), tmk, 0, it.h0, r, full_bar, pol);
+                tma_load_3d(smem_addr(sm.v[stage] + off), tmv, 0, it.h0, r, full_bar, pol);
+            }
+        } else {
+            // B < TB (B = 1) in the tensor-core layout: each token row
+            // goes by cp.async to its swizzled place (a TMA box of one
+            // row could not follow the swizzle).  Lanes 0-15 copy K and
+            // 16-31 V of token lane % 16; every lane's copies complete on
+            // the stage's full barrier (32 arrivals for these stages).
+            const int tk = lane & 15;
+            const int raw = __shfl_sync(FULL, cur, (pa - wbase + tk) & 31);   // page of token t + tk
+            if (tk < nt) {
+                const int id = checked(raw);
+                const size_t row = (size_t)(p.layer_row0 + id * B + (t + tk) % B);
+                const __half *src = (lane < 16 ? p.k_pool : p.v_pool) + (row * p.n_kv_heads + it.h0) * D;
+                uint8_t *dst = reinterpret_cast<uint8_t *>(lane < 16 ? sm.k[stage] : sm.v[stage]);
+#pragma unroll
+                for (int hl = 0; hl < HG; ++hl) {
+                    if (it.h0 + hl < p.n_kv_heads) {
+#pragma unroll
+                        for (int c = 0; c < D / 8; ++c)
+                            cp_async16_cg(smem_addr(dst + hl * (D / 64) * TB * 128 + swz(tk, c)), src + hl * D + c * 8);
+                    }
+                }
+            }
+            cp_async_mbar_arrive_noinc(full_bar);
+        }
+        ++st;
+        return true;
+    };
+
+    for (int k = 0; ok; ++k) {
         const int slot = k % NQ;
         if (!warp_wait(smem_addr(&sm.qempty[slot]), ((k / NQ) & 1) ^ 1, p.status, lane)) break;
         if (it.done) {
@@ -555,75 +640,13 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         // The next item's numbering and block ids are requested now; their
         // latency overlaps with issuing this item's tiles.
         const ProdItem nx = decode(k + 1);
-
-        int wbase = 0;
-        int cur = it.ids0;
-        int nxt = it.ids1;
         const int ntiles = (it.ntok + TB - 1) / TB;
-        for (int j = 0; j < ntiles; ++j, ++st) {
-            const int t = it.tok0 + j * TB;
-            const int nt = min(TB, it.tok0 + it.ntok - t);
-            const int pa = t / B - it.pg0;            // first page of the tile, item-relative
-            if (pa - wbase >= 32) {                    // move to the prefetched window
-                wbase += 32;
-                cur = nxt;
-                nxt = load_id(it.s, it.pg0, it.npg, wbase + 32);
-            }
-            const int stage = st % NS;
-            if (!warp_wait(smem_addr(&sm.empty[stage]), ((st / NS) & 1) ^ 1, p.status, lane)) {
-                ok = false;
-                break;
-            }
-            const uint32_t full_bar = smem_addr(&sm.full[stage]);
-            if (B >= TB) {
-                // the tile is rows [t % B, t % B + TB) of one page
-                const int id = checked(__shfl_sync(FULL, cur, pa - wbase));
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar, kTileBytes);
-                    const int r = p.layer_row0 + id * B + (t % B);
-                    tile_load<D, HG, MMA>(sm.k[stage], tmk, it.h0, r, full_bar, pol);
-                    tile_load<D, HG, MMA>(sm.v[stage], tmv, it.h0, r, full_bar, pol);
-                }
-            } else if constexpr (!MMA) {
-                // B < TB (B = 1): one box of B rows per page
-                const int pb = (t + nt - 1) / B - it.pg0;
-                const int np = pb - pa + 1;
-                const int raw = __shfl_sync(FULL, cur, (pa - wbase + lane) & 31);
-                if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)np * B * HG * D * 2 * 2);
-                __syncwarp();
-                if (lane < np) {
-                    const int r = p.layer_row0 + checked(raw) * B;
-                    const int off = lane * B * HG * D;
-                    tma_load_3d(smem_addr(sm.k[stage] + off), tmk, 0, it.h0, r, full_bar, pol);
-                    tma_load_3d(smem_addr(sm.v[stage] + off), tmv, 0, it.h0, r, full_bar, pol);
-                }
-            } else {
-                // B < TB (B = 1) in the tensor-core layout: each token row
-                // goes by cp.async to its swizzled place (a TMA box of one
-                // row could not follow the swizzle).  Lanes 0-15 copy K and
-                // 16-31 V of token lane % 16; every lane's copies complete on
-                // the stage's full barrier (32 arrivals for these stages).
-                const int tk = lane & 15;
-                const int raw = __shfl_sync(FULL, cur, (pa - wbase + tk) & 31);   // page of token t + tk
-                if (tk < nt) {
-                    const int id = checked(raw);
-                    const size_t row = (size_t)(p.layer_row0 + id * B + (t + tk) % B);
-                    const __half *src = (lane < 16 ? p.k_pool : p.v_pool) + (row * p.n_kv_heads + it.h0) * D;
-                    uint8_t *dst = reinterpret_cast<uint8_t *>(lane < 16 ? sm.k[stage] : sm.v[stage]);
-#pragma unroll
-                    for (int hl = 0; hl < HG; ++hl) {
-                        if (it.h0 + hl < p.n_kv_heads) {
-#pragma unroll
-                            for (int c = 0; c < D / 8; ++c)
-                                cp_async16_cg(smem_addr(dst + hl * (D / 64) * TB * 128 + swz(tk, c)), src + hl * D + c * 8);
-                        }
-                    }
-                }
-                cp_async_mbar_arrive_noinc(full_bar);
-            }
-        }
+        for (int j = 0; j < ntiles && ok; ++j) ok = issue_tile(j);
         if (!ok) break;
         it = nx;
+        wbase = 0;
+        cur = it.ids0;
+        nxt = it.ids1;
     }
 
     // Wait (bounded) for this CTA's last copies so none is in flight when the
@@ -679,8 +702,10 @@ __device__ __forceinline__ void store_whole(const Params &p, const ItemDesc &d, 
 }
 
 // Rows row0 .. row0 + R - 1 of the record of one part of a cut pair for head
-// hl (state as in store_whole, m and l the same in every lane); the first
-// part also writes the pair's job.
+// hl (state as in store_whole, m and l the same in every lane).  Chunk
+// schedule: fp32 words, and the first part also writes the pair's job.  Span
+// schedule: words tagged with the launch's epoch, record ((span * 2 + slot)
+// * HG + hl).
 template <int D, int G, int HG, int R>
 __device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG> &sm, const ItemDesc &d, int hl,
                                            int lane, int row0, bool write_job, const float (&m)[R],
@@ -688,7 +713,25 @@ __device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG>
     constexpr int LPT = D / 8;
     constexpr int REC = G * (D + 2);
     const int Hkv = p.n_kv_heads;
-    const size_t rec = d.kind == kChunk ? (size_t)d.a * Hkv + d.h0 + hl : ((size_t)d.span * 2 + d.c) * HG + hl;
+    if (d.kind == kSpanPart) {
+        unsigned long long *part = p.span_recs + (((size_t)d.span * 2 + d.c) * HG + hl) * REC;
+        if (lane < LPT) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int g = row0 + r;
+                if (g >= G) continue;
+                unsigned long long *w = part + g * (D + 2);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) st_tagged(w + lane * 8 + i, acc[r][i], p.epoch);
+                if (lane == 0) {
+                    st_tagged(w + D, m[r], p.epoch);
+                    st_tagged(w + D + 1, l[r], p.epoch);
+                }
+            }
+        }
+        return;
+    }
+    const size_t rec = (size_t)d.a * Hkv + d.h0 + hl;
     float *part = p.partials + rec * REC;
     if (lane < LPT) {
 #pragma unroll
@@ -719,24 +762,19 @@ __device__ __forceinline__ void write_part(const Params &p, const Smem<D, G, HG>
     }
 }
 
-// Merge the n_parts records of one cut pair for kv-head h (head hl of its
-// group) with the log-sum-exp rule and write its G output rows.  Chunk
-// records are (first + i) * Hkv + h; span records ((first + i) * 2 + slot) *
-// HG + hl, where only the first span can use slot 1 (z_first).  Each lane
+// Merge the n_parts records of one cut pair for kv-head h with the
+// log-sum-exp rule and write its G output rows (chunk schedule: records
+// (first + i) * Hkv + h, complete when the merge kernel runs).  Each lane
 // loads one part's (m, l) and, in the same round trip, every part's acc
 // values of its own dims (D / 32 of them), PB parts at a time.
 template <int D, int G, int HG>
-__device__ __forceinline__ void merge_pair(const Params &p, int kind, int first, int z_first, int n, int qrow0,
-                                           int nq, int h, int hl, int lane) {
+__device__ __forceinline__ void merge_pair(const Params &p, int first, int n, int qrow0, int nq, int h, int lane) {
     constexpr int REC = G * (D + 2);
     constexpr int DPL = D / 32;   // dims per lane
     constexpr int PB = 8;         // parts whose acc loads are in flight together
     const int Hkv = p.n_kv_heads;
     const int Hq = p.n_q_heads;
-    auto rec_of = [&](int i) -> size_t {
-        return kind == kChunk ? (size_t)(first + i) * Hkv + h
-                              : ((size_t)(first + i) * 2 + (i == 0 ? z_first : 0)) * HG + hl;
-    };
+    auto rec_of = [&](int i) -> size_t { return (size_t)(first + i) * Hkv + h; };
 #pragma unroll 1
     for (int g = 0; g < G; ++g) {
         const int qi = g / p.gh;                  // query token of row g
@@ -821,42 +859,118 @@ __device__ __forceinline__ void zero_empty_outputs(const Params &p, int cw, int 
     }
 }
 
-// Span schedule, when a consumer warp has no items left: count its cut parts
-// (record slots 0 / 1, bits of `pending`) in their pairs' arrivals.  One
-// fence releases the records (this warp's lanes wrote them before the
-// __syncwarp), then both increments are in flight together.  The part that
-// draws a pair's last count (n_parts * arrive of them) acquires and merges
-// the pair's records.
+// Span schedule: merge the n parts of a cut pair for kv-head h (head hl of
+// its group) and write its G output rows.  Part i is record ((first + i) * 2
+// + slot) * HG + hl, slot z_first for i = 0 (the pair may start inside its
+// first span, after that span's first segment) and 0 for the others.  Each
+// lane loads one part's (m, l) and, in the same round trip, every part's acc
+// values of its own dims (D / 32 of them), PB parts at a time; a batch is
+// loaded again (after a short sleep) until every word carries this launch's
+// epoch.  The parts are written by CTAs of earlier spans (and this warp),
+// which wait for no one, so the words arrive; the wait is bounded all the
+// same and gives up with PF_DEV_WAIT_TIMEOUT.
 template <int D, int G, int HG>
-__device__ __forceinline__ void count_pending(const Params &p, const PendPart (&pend)[2], int pending, int arrive,
-                                              int hl, int lane) {
+__device__ __forceinline__ bool merge_span_pair(const Params &p, int first, int z_first, int n, int qrow0, int nq,
+                                                int h, int hl, int lane) {
+    constexpr int REC = G * (D + 2);
+    constexpr int DPL = D / 32;   // dims per lane
+    constexpr int PB = 8;         // parts whose acc loads are in flight together
+    const int Hq = p.n_q_heads;
+    auto rec_of = [&](int i) -> const unsigned long long * {
+        return p.span_recs + (((size_t)(first + i) * 2 + (i == 0 ? z_first : 0)) * HG + hl) * REC;
+    };
+    unsigned long long t_wait = 0;   // when polling began (0: not yet)
+#pragma unroll 1
+    for (int g = 0; g < G; ++g) {
+        const int qi = g / p.gh;                  // query token of row g
+        if (qi >= nq) break;
+        float mx = -INFINITY, ls = 0.0f;
+        float a[DPL];
+#pragma unroll
+        for (int q = 0; q < DPL; ++q) a[q] = 0.0f;
+        for (int i0 = 0; i0 < n; i0 += 32) {
+            const int i = i0 + lane;
+            const int nb = min(32, n - i0);
+            float mi = -INFINITY, li = 0.0f;
+            for (int j0 = 0; j0 < nb; j0 += PB) {
+                float v[PB][DPL];
+                for (;;) {
+                    bool have = true;
+                    if (j0 == 0 && i < n) {
+                        const unsigned long long *pc = rec_of(i) + g * (D + 2);
+                        const unsigned long long wm = ld_tagged(pc + D), wl = ld_tagged(pc + D + 1);
+                        have = tagged_epoch(wm) == p.epoch && tagged_epoch(wl) == p.epoch;
+                        mi = tagged_value(wm);
+                        li = tagged_value(wl);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < PB; ++jj) {
+                        if (j0 + jj < nb) {
+                            const unsigned long long *pc = rec_of(i0 + j0 + jj) + g * (D + 2);
+#pragma unroll
+                            for (int q = 0; q < DPL; ++q) {
+                                const unsigned long long w = ld_tagged(pc + lane + 32 * q);
+                                have = have && tagged_epoch(w) == p.epoch;
+                                v[jj][q] = tagged_value(w);
+                            }
+                        }
+                    }
+                    if (__all_sync(FULL, have)) break;
+                    const unsigned long long now = global_timer_ns();
+                    if (t_wait == 0) {
+                        t_wait = now;
+                    } else if (now - t_wait > kWaitLimitNs) {
+                        if (lane == 0) atomicOr(p.status, PF_DEV_WAIT_TIMEOUT);
+                        return false;
+                    }
+                    __nanosleep(256);
+                }
+                // running reference over the batches of 32 parts
+                float bm = mi;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) bm = fmaxf(bm, __shfl_xor_sync(FULL, bm, o));
+                const float mn = fmaxf(mx, bm);
+                if (mn > mx) {
+                    const float sc = (mx == -INFINITY) ? 0.0f : exp2f(mx - mn);
+                    ls *= sc;
+#pragma unroll
+                    for (int q = 0; q < DPL; ++q) a[q] *= sc;
+                    mx = mn;
+                }
+                const float w = (i < n && j0 == 0) ? exp2f(mi - mx) : 0.0f;
+                if (j0 == 0) ls = fmaf(w, li, ls);
+#pragma unroll
+                for (int jj = 0; jj < PB; ++jj) {
+                    const float wj = __shfl_sync(FULL, exp2f(mi - mx), j0 + jj);
+                    if (j0 + jj < nb) {
+#pragma unroll
+                        for (int q = 0; q < DPL; ++q) a[q] = fmaf(wj, v[jj][q], a[q]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ls += __shfl_xor_sync(FULL, ls, o);
+        const float inv = 1.0f / ls;
+#pragma unroll
+        for (int q = 0; q < DPL; ++q) {
+            const size_t o = ((size_t)(qrow0 + qi) * Hq + (size_t)h * p.gh + g - qi * p.gh) * D + lane + 32 * q;
+            if (p.out_f32) static_cast<float *>(p.out)[o] = a[q] * inv;
+            else static_cast<__half *>(p.out)[o] = __float2half_rn(a[q] * inv);
+        }
+    }
+    return true;
+}
+
+// Span schedule, when a consumer warp has no items left: its CTA merges the
+// cut pair whose last part is its span's first segment (record slot 0, bit 0
+// of `pending`).  A part in slot 1 (a pair that starts inside the span and
+// runs past its end) is merged by a later span.
+template <int D, int G, int HG>
+__device__ __forceinline__ void merge_if_last(const Params &p, const PendPart &pp, int pending, int hl, int lane) {
+    if (!(pending & 1) || pp.first + pp.n_parts - 1 != (int)blockIdx.x) return;
     __syncwarp();
-    unsigned got0 = 0, got1 = 0;
-    if (lane == 0) {
-        fence_acq_rel_gpu();
-        if (pending & 1)
-            got0 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pend[0].first * HG + hl,
-                                          (unsigned)(pend[0].n_parts * arrive - 1));
-        if (pending & 2)
-            got1 = atomic_inc_relaxed_gpu(p.arrivals + (size_t)pend[1].first * HG + hl,
-                                          (unsigned)(pend[1].n_parts * arrive - 1));
-    }
-    got0 = __shfl_sync(FULL, got0, 0);
-    got1 = __shfl_sync(FULL, got1, 0);
-    const PendPart pp0 = pend[0];
-    const PendPart pp1 = pend[1];
-    const bool last0 = (pending & 1) && got0 == (unsigned)(pp0.n_parts * arrive - 1);
-    const bool last1 = (pending & 2) && got1 == (unsigned)(pp1.n_parts * arrive - 1);
-    if (last0 || last1) {
-        if (lane == 0) fence_acq_rel_gpu();
-        __syncwarp();
-        if (last0)
-            merge_pair<D, G, HG>(p, kSpanPart, pp0.first, pp0.z_first, pp0.n_parts, pp0.qrow0, pp0.nq, pp0.h0 + hl,
-                                 hl, lane);
-        if (last1)
-            merge_pair<D, G, HG>(p, kSpanPart, pp1.first, pp1.z_first, pp1.n_parts, pp1.qrow0, pp1.nq, pp1.h0 + hl,
-                                 hl, lane);
-    }
+    merge_span_pair<D, G, HG>(p, pp.first, pp.z_first, pp.n_parts, pp.qrow0, pp.nq, pp.h0 + hl, hl, lane);
 }
 
 // Span schedule: note a finished cut part (lane 0; written to the warp's
@@ -888,7 +1002,6 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
     // otherwise they split each tile's tokens and merge at the end.
     constexpr bool RSPLIT = WPH > 1 && G >= WPH;
     constexpr int R = RSPLIT ? (G + WPH - 1) / WPH : G;   // rows this warp holds
-    constexpr int ARRIVE = RSPLIT ? WPH : 1;             // a cut part's arrivals per head
     constexpr int TPT = RSPLIT ? TB : TB / WPH;          // tokens of a tile this warp serves
     constexpr int STEPS = TPT / TPW;
     static_assert(STEPS * TPW == TPT, "tile must split into whole warp-steps");
@@ -904,13 +1017,13 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
     uint32_t st = 0;
     uint32_t cphase = 0;
     const uint32_t cbar = smem_addr(&sm.cbar);
-    int pending = 0;   // span schedule: bit c = a cut part with record slot c awaits its count
+    int pending = 0;   // span schedule: bit c = this warp wrote a cut part's record in slot c
     for (int k = 0;; ++k) {
         const int slot = k % NQ;
         if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
         const ItemDesc d = sm.desc[slot];
         if (d.s < 0) {
-            if (pending) count_pending<D, G, HG>(p, sm.pend[cw], pending, ARRIVE, hl, lane);
+            if (part == 0) merge_if_last<D, G, HG>(p, sm.pend[cw][0], pending, hl, lane);
             return;
         }
         const int h = d.h0 + hl;
@@ -1121,8 +1234,8 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                 // chunk 0 of the sequence also writes the merge job
                 write_part<D, G, HG, R>(p, sm, d, hl, lane, row0, d.b == 0 && hl == 0 && part == 0, m, l, acc);
             } else {
-                // Span part: write the record and note the pair; it is
-                // counted when this CTA has no items left.
+                // Span part: write the record and note the pair; the CTA
+                // of its last span merges it.
                 write_part<D, G, HG, R>(p, sm, d, hl, lane, row0, false, m, l, acc);
                 if (lane == 0) sm.pend[cw][d.c] = pending_part(p, sm.pre, d);
                 pending |= 1 << d.c;
@@ -1175,13 +1288,13 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
     uint32_t st = 0;
     uint32_t cphase = 0;
     const uint32_t cbar = smem_addr(&sm.cbar);
-    int pending = 0;   // span schedule: bit c = a cut part with record slot c awaits its count
+    int pending = 0;   // span schedule: bit c = this warp wrote a cut part's record in slot c
     for (int k = 0;; ++k) {
         const int slot = k % NQ;
         if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
         const ItemDesc d = sm.desc[slot];
         if (d.s < 0) {
-            if (pending) count_pending<D, G, HG>(p, sm.pend[cw], pending, 1, hl, lane);
+            merge_if_last<D, G, HG>(p, sm.pend[cw][0], pending, hl, lane);
             return;
         }
         const int h = d.h0 + hl;
@@ -1406,20 +1519,24 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                 for (int b = 0; b < NNB; ++b) store2(p, ob + b * 8, o[b][2 * r] * inv, o[b][2 * r + 1] * inv);
             }
         } else {
-            // Span part: write the record ((span * 2 + slot) * HG + head)
-            // and note the pair; it is counted when this CTA has no items left.
-            float *part_rec = p.partials + (((size_t)d.span * 2 + d.c) * HG + hl) * (size_t)(G * (D + 2));
+            // Span part: write the record ((span * 2 + slot) * HG + head),
+            // every word tagged with the launch's epoch, and note the pair;
+            // the CTA of its last span merges it.
+            unsigned long long *part_rec =
+                p.span_recs + (((size_t)d.span * 2 + d.c) * HG + hl) * (size_t)(G * (D + 2));
 #pragma unroll
             for (int r = 0; r < 2; ++r) {
                 const int g = gq + 8 * r;
                 if (g >= G) continue;
-                float *rw = part_rec + g * (D + 2);
+                unsigned long long *rw = part_rec + g * (D + 2);
 #pragma unroll
-                for (int b = 0; b < NNB; ++b)
-                    *reinterpret_cast<float2 *>(rw + b * 8 + 2 * tq) = make_float2(o[b][2 * r], o[b][2 * r + 1]);
+                for (int b = 0; b < NNB; ++b) {
+                    st_tagged(rw + b * 8 + 2 * tq, o[b][2 * r], p.epoch);
+                    st_tagged(rw + b * 8 + 2 * tq + 1, o[b][2 * r + 1], p.epoch);
+                }
                 if (tq == 0) {
-                    rw[D] = m[r];
-                    rw[D + 1] = l[r];
+                    st_tagged(rw + D, m[r], p.epoch);
+                    st_tagged(rw + D + 1, l[r], p.epoch);
                 }
             }
             if (lane == 0) sm.pend[cw][d.c] = pending_part(p, sm.pre, d);
@@ -1498,10 +1615,21 @@ __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const C
         if (lane == 31) sm.warp_tot[warp] = incl;
         __syncthreads();
         int run = incl - local;
-        for (int w = 0; w < warp; ++w) run += sm.warp_tot[w];
+        long long units = 0;   // per group, all sequences
+#pragma unroll
+        for (int w = 0; w < NTHREADS / 32; ++w) {
+            if (w < warp) run += sm.warp_tot[w];
+            units += sm.warp_tot[w];
+        }
+        // Each thread finds whether its sequences hold this CTA's first unit
+        // (x0), so the producer starts without a search.
+        const long long ng = p.n_groups;
+        const long long x0 = SpanMap(units * ng, gridDim.x).start(blockIdx.x);
         for (int i = lo; i < hi; ++i) {
+            const int before = run;
             run += sm.pre[i];
             sm.pre[i] = run;
+            if (before * ng <= x0 && x0 < run * ng) sm.s_first = i - 1;   // sequence i - 1: units [before, run)
         }
         if (threadIdx.x == 0) sm.pre[0] = 0;
     }
@@ -1572,7 +1700,7 @@ __global__ void __launch_bounds__(128, 1) merge_kernel(const Params p, int n_job
             qrow0 = p.cu_q[jb.s];
             nq = max(1, min(p.cu_q[jb.s + 1] - qrow0, p.rows / p.gh));
         }
-        merge_pair<D, G, HG>(p, jb.kind, jb.first, jb.z_first, jb.n_parts, qrow0, nq, jb.h0 + hl, hl, lane);
+        merge_pair<D, G, HG>(p, jb.first, jb.n_parts, qrow0, nq, jb.h0 + hl, lane);
     }
 }
 

@@ -44,24 +44,6 @@ int scratch_for_current_device(void **out) {
 }
 
 }  // namespace
-
-int noalloc_scratch_reset(cudaStream_t stream) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_error(e, "noalloc scratch reset: cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return PF_OK;
-    void *ptr = nullptr;
-    {
-        std::lock_guard<std::mutex> lock(g_scratch_mu);
-        ptr = g_scratch_ptr[dev];
-    }
-    if (!ptr) return PF_OK;   // never used on this device: still all zero
-    e = cudaMemsetAsync(ptr, 0, kNoAllocScratchBytes, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return cuda_error(e, "noalloc scratch reset");
-    return PF_OK;
-}
-
 }  // namespace pkv
 
 extern "C" int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer, const void *q,
@@ -82,11 +64,10 @@ extern "C" int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
     void *ws = nullptr;
     int rc = pkv::scratch_for_current_device(&ws);
     if (rc) return rc;
-    // The scratch is zero when the library loads.  Partial records are
-    // written before they are read, every merge job carries its own launch's
-    // epoch, and arrival counters return to zero by the end of every call
-    // that completes (after one that timed out, pf_device_status with reset
-    // zeroes the scratch again).
+    // The scratch is zero when the library loads.  Every word a call reads
+    // back (merge jobs, span records) carries the epoch of the launch that
+    // wrote it, so nothing left by an earlier call -- one that timed out
+    // included -- is taken for this call's data, and nothing needs resetting.
     return pf_paged_decode_attention(pool, layer, q, block_tables, max_blocks_per_seq, context_lens, n_seqs,
                                      n_q_heads, scale, out, out_dtype, split_tokens, ws, pkv::kNoAllocScratchBytes,
                                      stream);

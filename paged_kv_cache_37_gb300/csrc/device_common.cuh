@@ -121,6 +121,25 @@ __device__ __forceinline__ unsigned atomic_inc_relaxed_gpu(unsigned *p, unsigned
 
 __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 
+// One 64-bit word of a record shared between CTAs: the value's bits in the
+// low half and the writing launch's epoch in the high half, stored and loaded
+// as single 64-bit relaxed GPU-scope accesses (each indivisible), so a reader
+// that finds the current epoch in a word holds that launch's value, with no
+// fence on either side.
+__device__ __forceinline__ void st_tagged(unsigned long long *p, float v, unsigned epoch) {
+    const unsigned long long w = (unsigned long long)__float_as_uint(v) | ((unsigned long long)epoch << 32);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long *p) {
+    unsigned long long w;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+    return w;
+}
+
+__device__ __forceinline__ float tagged_value(unsigned long long w) { return __uint_as_float((unsigned)w); }
+__device__ __forceinline__ unsigned tagged_epoch(unsigned long long w) { return (unsigned)(w >> 32); }
+
 // 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
 // Both addresses 16-byte aligned, bytes a multiple of 16.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar) {

@@ -52,9 +52,6 @@ namespace pkv {
 // Device status word of the current device (a __device__ variable of this
 // library); kernels OR pf_device_flag bits into it.
 int *device_status_ptr();
-// Zero the no-allocation entry point's scratch on the current device, if that
-// entry point has used it (synchronous on the stream).
-int noalloc_scratch_reset(cudaStream_t stream);
 
 // TMA descriptors of the pool for boxes of hg (1, 2 or 4) kv-heads, or (hg
 // = 0) the tensor-core layout, on `device`, encoded on first use; *index
@@ -124,8 +121,7 @@ struct AttnPlan {
     int chunk;             // chunk schedule: tokens per chunk
     int grid;              // persistent grid (0 when planned without a device)
     size_t counter_bytes;  // reserved bytes at the front of the workspace (256 B)
-    size_t partial_bytes;  // fp32 partial records, then arrival counters, then merge jobs
-    size_t arrival_bytes;  // span schedule: one u32 per (span, head of a group)
+    size_t partial_bytes;  // partial records (spans: epoch-tagged 64-bit words; chunks: fp32), then merge jobs
     size_t n_jobs;         // chunk schedule: merge job slots (0: no merge kernel)
 };
 int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_blocks, int split_tokens,
