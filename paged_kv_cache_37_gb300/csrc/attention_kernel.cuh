@@ -196,17 +196,29 @@ struct Shape {
 };
 
 // Tensor-core consumers (HG kv-heads per item, each head's tiles dealt
-// round-robin to its NCW / HG consumer warps): the ring takes what is left
-// of a CTA's share of the SM's 228 KB -- 3 CTAs per SM at head_dim 64, 2 at
-// 128 -- after the fixed part (q slots, new rows, the warps' merge area, the
-// span tables, barriers), between 2 and 16 stages.
+// round-robin to its NCW / HG consumer warps): a stage holds SUB consecutive
+// 16-token tiles of one item behind one full/empty barrier pair, so that a
+// stage is at least kMmaStageMinBytes (with few kv-heads per item a tile is
+// small, and a barrier round trip and a producer turn per tile would bound
+// the rate).  The ring takes what is left of a CTA's share of the SM's
+// 228 KB -- 3 CTAs per SM at head_dim 64, 2 at 128 -- after the fixed part
+// (q slots, new rows, the warps' merge area, the span tables, barriers),
+// between 2 and 16 stages.
+#ifndef PKV_MMA_STAGE_MIN_BYTES
+#define PKV_MMA_STAGE_MIN_BYTES 16384
+#endif
+constexpr int kMmaStageMinBytes = PKV_MMA_STAGE_MIN_BYTES;
 template <int D, int G, int HG>
 struct MmaShape {
-    static constexpr int STAGE_BYTES = 2 * TB * HG * D * 2;
+    static constexpr int TILE_BYTES = 2 * TB * HG * D * 2;   // K and V of one tile
     static constexpr int BUDGET = (D == 64 ? 228 * 1024 / 3 : 228 * 1024 / 2) - 2048;   // reserved + alignment slack
     static constexpr bool MERGE = NCW / HG > 1;   // several warps per head meet in shared memory
     static constexpr int FIXED = NQ * HG * G * D * 2 + NQ * 2 * HG * D * 2 + (MERGE ? NCW : 1) * G * (D + 2) * 4 +
                                  (kMaxSeqsPerLaunch + 1) * 4 + kMaxSeqsPerLaunch + 1024;   // + barriers, items
+    static constexpr int SUB_WANT = TILE_BYTES >= kMmaStageMinBytes ? 1 : kMmaStageMinBytes / TILE_BYTES;
+    static constexpr int SUB_FIT = (BUDGET - FIXED) / (2 * TILE_BYTES);   // at least two stages
+    static constexpr int SUB = SUB_WANT < SUB_FIT ? SUB_WANT : (SUB_FIT < 1 ? 1 : SUB_FIT);
+    static constexpr int STAGE_BYTES = SUB * TILE_BYTES;
     static constexpr int NS_RAW = (BUDGET - FIXED) / STAGE_BYTES;
     static constexpr int NS = NS_RAW < 2 ? 2 : (NS_RAW > 16 ? 16 : NS_RAW);
 };
@@ -217,8 +229,9 @@ struct MmaShape {
 template <int D, int G, int HG, bool MMA = false>
 struct __align__(128) Smem {
     static constexpr int NS = MMA ? MmaShape<D, G, HG>::NS : Shape<D, HG>::NS;
-    __half k[NS][Shape<D, HG>::STAGE_HALVES];
-    __half v[NS][Shape<D, HG>::STAGE_HALVES];
+    static constexpr int SUB = MMA ? MmaShape<D, G, HG>::SUB : 1;   // tiles per stage
+    __half k[NS][SUB * Shape<D, HG>::STAGE_HALVES];
+    __half v[NS][SUB * Shape<D, HG>::STAGE_HALVES];
     __half q[NQ][HG * G * D];
     __half knew[NQ][2][HG * D];   // fused step: the new token's K and V rows of the item's heads
     float red[(MMA ? MmaShape<D, G, HG>::MERGE : Shape<D, HG>::WPH > 1) ? NCW : 1][G][D + 2];   // per consumer warp: acc[D], m, l
@@ -514,65 +527,76 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     int wbase = 0;
     int cur = it.ids0;
     int nxt = it.ids1;
-    // Issue tile j of the current item into the next stage (st); false when
-    // the wait for the stage gave up.
-    auto issue_tile = [&](int j) -> bool {
-        const int t = it.tok0 + j * TB;
-        const int nt = min(TB, it.tok0 + it.ntok - t);
-        const int pa = t / B - it.pg0;            // first page of the tile, item-relative
-        if (pa - wbase >= 32) {                    // move to the prefetched window
-            wbase += 32;
-            cur = nxt;
-            nxt = load_id(it.s, it.pg0, it.npg, wbase + 32);
-        }
+    // Issue tiles j0 .. j0 + SUB - 1 of the current item (those it has) into
+    // the next stage (st), at SUBH halves apart; false when the wait for the
+    // stage gave up.
+    constexpr int SUB = Smem<D, G, HG, MMA>::SUB;
+    constexpr int SUBH = Shape<D, HG>::STAGE_HALVES;
+    auto issue_stage = [&](int j0) -> bool {
+        const int nsub = min(SUB, (it.ntok + TB - 1) / TB - j0);
         const int stage = st % NS;
         if (!warp_wait(smem_addr(&sm.empty[stage]), ((st / NS) & 1) ^ 1, p.status, lane)) return false;
         const uint32_t full_bar = smem_addr(&sm.full[stage]);
         if (B >= TB) {
-            // the tile is rows [t % B, t % B + TB) of one page
-            const int id = checked(__shfl_sync(FULL, cur, pa - wbase));
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full_bar, kTileBytes);
-                const int r = p.layer_row0 + id * B + (t % B);
-                tile_load<D, HG, MMA>(sm.k[stage], tmk, it.h0, r, full_bar, pol);
-                tile_load<D, HG, MMA>(sm.v[stage], tmv, it.h0, r, full_bar, pol);
+            if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)nsub * kTileBytes);
+        }
+        for (int u = 0; u < nsub; ++u) {
+            const int t = it.tok0 + (j0 + u) * TB;
+            const int nt = min(TB, it.tok0 + it.ntok - t);
+            const int pa = t / B - it.pg0;            // first page of the tile, item-relative
+            if (pa - wbase >= 32) {                    // move to the prefetched window
+                wbase += 32;
+                cur = nxt;
+                nxt = load_id(it.s, it.pg0, it.npg, wbase + 32);
             }
-        } else if constexpr (!MMA) {
-            // B < TB (B = 1): one box of B rows per page
-            const int pb = (t + nt - 1) / B - it.pg0;
-            const int np = pb - pa + 1;
-            const int raw = __shfl_sync(FULL, cur, (pa - wbase + lane) & 31);
-            if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)np * B * HG * D * 2 * 2);
-            __syncwarp();
-            if (lane < np) {
-                const int r = p.layer_row0 + checked(raw) * B;
-                const int off = lane * B * HG * D;
-                tma_load_3d(smem_addr(sm.k[stage] + off), tmk, 0, it.h0, r, full_bar, pol);
-                tma_load_3d(smem_addr(sm.v[stage] + off), tmv, 0, it.h0, r, full_bar, pol);
-            }
-        } else {
-            // B < TB (B = 1) in the tensor-core layout: each token row
-            // goes by cp.async to its swizzled place (a TMA box of one
-            // row could not follow the swizzle).  Lanes 0-15 copy K and
-            // 16-31 V of token lane % 16; every lane's copies complete on
-            // the stage's full barrier (32 arrivals for these stages).
-            const int tk = lane & 15;
-            const int raw = __shfl_sync(FULL, cur, (pa - wbase + tk) & 31);   // page of token t + tk
-            if (tk < nt) {
-                const int id = checked(raw);
-                const size_t row = (size_t)(p.layer_row0 + id * B + (t + tk) % B);
-                const __half *src = (lane < 16 ? p.k_pool : p.v_pool) + (row * p.n_kv_heads + it.h0) * D;
-                uint8_t *dst = reinterpret_cast<uint8_t *>(lane < 16 ? sm.k[stage] : sm.v[stage]);
+            if (B >= TB) {
+                // the tile is rows [t % B, t % B + TB) of one page
+                const int id = checked(__shfl_sync(FULL, cur, pa - wbase));
+                if (lane == 0) {
+                    const int r = p.layer_row0 + id * B + (t % B);
+                    tile_load<D, HG, MMA>(sm.k[stage] + u * SUBH, tmk, it.h0, r, full_bar, pol);
+                    tile_load<D, HG, MMA>(sm.v[stage] + u * SUBH, tmv, it.h0, r, full_bar, pol);
+                }
+            } else if constexpr (!MMA) {
+                // B < TB (B = 1): one box of B rows per page (one tile per stage)
+                const int pb = (t + nt - 1) / B - it.pg0;
+                const int np = pb - pa + 1;
+                const int raw = __shfl_sync(FULL, cur, (pa - wbase + lane) & 31);
+                if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)np * B * HG * D * 2 * 2);
+                __syncwarp();
+                if (lane < np) {
+                    const int r = p.layer_row0 + checked(raw) * B;
+                    const int off = lane * B * HG * D;
+                    tma_load_3d(smem_addr(sm.k[stage] + off), tmk, 0, it.h0, r, full_bar, pol);
+                    tma_load_3d(smem_addr(sm.v[stage] + off), tmv, 0, it.h0, r, full_bar, pol);
+                }
+            } else {
+                // B < TB (B = 1) in the tensor-core layout: each token row
+                // goes by cp.async to its swizzled place (a TMA box of one
+                // row could not follow the swizzle).  Lanes 0-15 copy K and
+                // 16-31 V of token lane % 16.
+                const int tk = lane & 15;
+                const int raw = __shfl_sync(FULL, cur, (pa - wbase + tk) & 31);   // page of token t + tk
+                if (tk < nt) {
+                    const int id = checked(raw);
+                    const size_t row = (size_t)(p.layer_row0 + id * B + (t + tk) % B);
+                    const __half *src = (lane < 16 ? p.k_pool : p.v_pool) + (row * p.n_kv_heads + it.h0) * D;
+                    uint8_t *dst = reinterpret_cast<uint8_t *>((lane < 16 ? sm.k[stage] : sm.v[stage]) + u * SUBH);
 #pragma unroll
-                for (int hl = 0; hl < HG; ++hl) {
-                    if (it.h0 + hl < p.n_kv_heads) {
+                    for (int hl = 0; hl < HG; ++hl) {
+                        if (it.h0 + hl < p.n_kv_heads) {
 #pragma unroll
-                        for (int c = 0; c < D / 8; ++c)
-                            cp_async16_cg(smem_addr(dst + hl * (D / 64) * TB * 128 + swz(tk, c)), src + hl * D + c * 8);
+                            for (int c = 0; c < D / 8; ++c)
+                                cp_async16_cg(smem_addr(dst + hl * (D / 64) * TB * 128 + swz(tk, c)), src + hl * D + c * 8);
+                        }
                     }
                 }
             }
-            cp_async_mbar_arrive_noinc(full_bar);
+        }
+        // cp.async stages: every lane's copies complete on the stage's full
+        // barrier (32 arrivals for these stages)
+        if constexpr (MMA) {
+            if (B < TB) cp_async_mbar_arrive_noinc(full_bar);
         }
         ++st;
         return true;
@@ -642,7 +666,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
         // latency overlaps with issuing this item's tiles.
         const ProdItem nx = decode(k + 1);
         const int ntiles = (it.ntok + TB - 1) / TB;
-        for (int j = 0; j < ntiles && ok; ++j) ok = issue_tile(j);
+        for (int j = 0; j < ntiles && ok; j += SUB) ok = issue_stage(j);
         if (!ok) break;
         it = nx;
         wbase = 0;
@@ -1271,6 +1295,8 @@ __device__ __forceinline__ void store2(const Params &p, size_t o, float x0, floa
 template <int D, int G, int HG>
 __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, true> &sm, int cw, int lane) {
     constexpr int NS = Smem<D, G, HG, true>::NS;
+    constexpr int SUB = Smem<D, G, HG, true>::SUB;   // tiles per stage
+    constexpr int SUBH = Shape<D, HG>::STAGE_HALVES;   // halves of one tile's K (or V)
     constexpr int WPH = NCW / HG;   // consumer warps per head
     constexpr int NKS = D / 16;     // k-steps of the score product
     constexpr int NNB = D / 8;      // 8-dim column blocks of O
@@ -1346,12 +1372,15 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
         for (int b = 0; b < NNB; ++b) o[b][0] = o[b][1] = o[b][2] = o[b][3] = 0.0f;
 
         const int ntiles = (d.ntok + TB - 1) / TB;
-        for (int j = 0; j < ntiles; ++j, ++st) {
+        for (int j0 = 0; j0 < ntiles; j0 += SUB, ++st) {
             const int stage = st % NS;
             if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane)) return;
+            const int nsub = min(SUB, ntiles - j0);
+            for (int u = 0; u < nsub; ++u) {
+            const int j = j0 + u;   // tile of the item; the stage holds tile j at u * SUBH halves
             if (active && (j % WPH) == part) {
-                uint8_t *kt = reinterpret_cast<uint8_t *>(sm.k[stage]) + hoff;
-                uint8_t *vt = reinterpret_cast<uint8_t *>(sm.v[stage]) + hoff;
+                uint8_t *kt = reinterpret_cast<uint8_t *>(sm.k[stage] + u * SUBH) + hoff;
+                uint8_t *vt = reinterpret_cast<uint8_t *>(sm.v[stage] + u * SUBH) + hoff;
                 const uint32_t kb = smem_addr(kt);
                 const uint32_t vb = smem_addr(vt);
                 const int tile0 = d.tok0 + j * TB;
@@ -1443,6 +1472,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                     mma_f16_16816(o[2 * np], pa, b[0], b[1]);
                     mma_f16_16816(o[2 * np + 1], pa, b[2], b[3]);
                 }
+            }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_addr(&sm.empty[stage]));
