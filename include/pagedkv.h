@@ -243,13 +243,20 @@ PF_API int pf_decode_workspace_init(void *workspace, size_t ws_bytes, void *stre
  * or PF_F32); n_q_heads must be a multiple of Hkv (grouped heads share one
  * page load): 1 to 8 q-heads per kv-head under any split setting, up to 16
  * with split_tokens = 0 on pages of at least 16 tokens (PF_ERR_UNSUPPORTED
- * otherwise).  With split_tokens = 0 and such pages the scores and the
- * weighted sum are computed on tensor cores with the weights rounded to fp16
- * (within the same tolerance of the exact result); fixed chunks keep fp32
- * weights.  Sequences longer than split_tokens are cut into chunks whose
- * partial results are combined with the log-sum-exp rule (same section:
- * reduction across thread blocks); split_tokens 0 = choose automatically,
- * -1 = never split, > 0 = chunk length (rounded up to a multiple of 16).
+ * otherwise).  Schedules: split_tokens 0 = balanced spans (the work of all
+ * sequences cut into equal shares, one per resident block; a sequence cut
+ * by a share boundary has its partial results combined with the log-sum-exp
+ * rule -- same section: reduction across thread blocks); -2 = the same
+ * spans on the CUDA cores; -1 = never split; > 0 = fixed chunks of that
+ * many tokens (rounded up to a multiple of 16), combined the same way.
+ * Arithmetic: fp32 throughout, inputs fp16.  split_tokens 0 computes the
+ * score and weighted-sum products on tensor cores (fp16 operands, fp32
+ * accumulation); for fp16 output the softmax weights enter the weighted sum
+ * rounded to fp16 (within the attention tolerance of the exact result), for
+ * fp32 output as an fp16 part plus its fp16 rounding error (about 22 bits,
+ * like the other schedules).  Every other schedule uses CUDA-core fp32
+ * arithmetic (warp-shuffle dot products, fp32 weights) and no tensor
+ * cores.
  * workspace: device memory of at least pf_decode_workspace_bytes(...) bytes,
  * initialised once with pf_decode_workspace_init; calls sharing a workspace
  * must not overlap on the GPU. */
@@ -369,6 +376,19 @@ PF_API int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
                                              float scale, void *out,
                                              int out_dtype, int split_tokens,
                                              void *stream);
+
+/* Testing hook for the bounded waits (no counterpart on the pages): the next
+ * decode-attention launch in this process (pf_paged_decode_attention,
+ * pf_decode_step, the noalloc variant, or the decode-kernel path of
+ * pf_paged_prefill_attention) runs with a 2 ms wait limit instead of 1 s, and
+ * its block 0 leaves the first stage of its copy ring unfilled.  The waits
+ * for that stage, and the merge of any split sequence with a part in block
+ * 0, give up after the limit: the kernel sets PF_DEV_WAIT_TIMEOUT, every
+ * block returns (after its own copies in flight have landed), and the
+ * context stays usable.  That launch's output is undefined; the next launch
+ * with the same workspace computes normally.  Nothing is faulted and no
+ * memory is touched out of bounds.  Always PF_OK. */
+PF_API int pf_test_inject_wait_timeout(void);
 
 /* Read the device status word (OR of pf_device_flag bits set by kernels of
  * this library on the current device since the last reset) into *status_out.

@@ -18,6 +18,7 @@ from ._native import (  # noqa: F401
     pf_alloc_refcount, pf_alloc_share, pf_block_image_bytes, pf_copy_blocks, pf_seq_fork, pf_swap_in,
     pf_swap_out,
     pf_decode_step, pf_decode_workspace_bytes, pf_decode_workspace_init, pf_device_status, pf_free_blocks,
+    pf_test_inject_wait_timeout,
     pf_gather_kv, pf_last_error, pf_paged_decode_attention, pf_paged_decode_attention_noalloc,
     pf_paged_prefill_attention, pf_prefill_workspace_bytes,
     pf_pool_bytes, pf_pool_create,

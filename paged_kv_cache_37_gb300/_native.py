@@ -91,6 +91,7 @@ def lib():
         "pf_decode_workspace_init": (I, [P, Z, P]),
         "pf_paged_decode_attention": (I, [P, I, P, P, I, P, I, I, F, P, I, I, P, Z, P]),
         "pf_device_status": (I, [ctypes.POINTER(I), I, P]),
+        "pf_test_inject_wait_timeout": (I, []),
         "pf_paged_decode_attention_noalloc": (I, [P, I, P, P, I, P, I, I, F, P, I, I, P]),
         "pf_decode_step": (I, [P, I, P, P, P, P, I, P, I, I, F, P, I, I, P, Z, I, P]),
     }
@@ -441,6 +442,13 @@ def pf_paged_decode_attention_noalloc(pool, layer, q, block_tables, context_lens
         pool.handle, layer, _dev_ptr(q, "q", torch.float16), _dev_ptr(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev_ptr(context_lens, "context_lens", torch.int32), n, hq, float(scale),
         _dev_ptr(out, "out"), out_dtype, split_tokens, _stream_ptr(stream)))
+
+
+def pf_test_inject_wait_timeout():
+    """Testing hook: the next decode-attention launch leaves one stage of its
+    copy ring unfilled and waits 2 ms for it before giving up (see the C
+    header)."""
+    _check(lib().pf_test_inject_wait_timeout())
 
 
 def pf_device_status(reset=False, stream=None):

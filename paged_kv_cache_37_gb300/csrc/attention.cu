@@ -135,10 +135,13 @@ namespace {
 
 // The kernel for G = n_q_heads / n_kv_heads rows per kv-head: *hg its
 // kv-heads per item, *mma whether it has the tensor-core consumers (one
-// kv-head per item, its tensor map the swizzled one).
-int kernel_for(const pf_pool *pool, int n_q_heads, bool spans, KernelInfo *ki, int *hg, bool *mma) {
+// kv-head per item, its tensor map the swizzled one).  The tensor-core
+// consumers serve the balanced schedule unless the call asks for the CUDA
+// cores.
+int kernel_for(const pf_pool *pool, int n_q_heads, bool spans, bool cuda_cores, KernelInfo *ki, int *hg,
+               bool *mma) {
     const int G = n_q_heads / pool->n_kv_heads;
-    *mma = spans && G >= mma_min_rows(pool->head_dim) && G <= kMmaMaxRows;
+    *mma = spans && !cuda_cores && G >= mma_min_rows(pool->head_dim) && G <= kMmaMaxRows;
     if (*mma) {
         *hg = mma_heads(pool->n_kv_heads, G, pool->head_dim);
         *ki = kernel_mma(pool->head_dim, G, *hg);
@@ -151,11 +154,11 @@ int kernel_for(const pf_pool *pool, int n_q_heads, bool spans, KernelInfo *ki, i
 }
 
 // Persistent grid of the kernel on the current device: SMs x resident CTAs.
-int resident_grid(const pf_pool *pool, int n_q_heads, bool spans, int *grid) {
+int resident_grid(const pf_pool *pool, int n_q_heads, bool spans, bool cuda_cores, int *grid) {
     KernelInfo ki;
     int HG = 0;
     bool mma = false;
-    int rc = kernel_for(pool, n_q_heads, spans, &ki, &HG, &mma);
+    int rc = kernel_for(pool, n_q_heads, spans, cuda_cores, &ki, &HG, &mma);
     if (rc) return rc;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -194,6 +197,11 @@ unsigned next_epoch() {
 // Grid bound used to size span records when no device can be queried.
 constexpr int kGridBoundNoDevice = 4096;
 
+// pf_test_inject_wait_timeout: the next launch runs with a short wait limit
+// and block 0 leaves its first ring stage unfilled.
+std::atomic<int> g_inject_timeout{0};
+constexpr unsigned long long kInjectedWaitLimitNs = 2000000ull;   // 2 ms
+
 
 
 }  // namespace
@@ -204,13 +212,14 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
     const long long cap = (maxctx + TB - 1) / TB * TB;
     if (cap > (1ll << 30))
         return set_error(PF_ERR_INVALID, "attention: max_blocks_per_seq * block_size is too large");
-    if (split_tokens < -1)
-        return set_error(PF_ERR_INVALID, "attention: split_tokens must be -1, 0 or positive");
+    if (split_tokens < -2)
+        return set_error(PF_ERR_INVALID, "attention: split_tokens must be -2, -1, 0 or positive");
     KernelInfo ki;
     int HG = 0;
     bool mma = false;
-    plan->spans = split_tokens == 0;
-    int rc = kernel_for(pool, n_q_heads, plan->spans, &ki, &HG, &mma);
+    plan->spans = split_tokens == 0 || split_tokens == -2;
+    plan->cuda_cores = split_tokens != 0;
+    int rc = kernel_for(pool, n_q_heads, plan->spans, plan->cuda_cores, &ki, &HG, &mma);
     if (rc) return rc;
     // a record: the rows of the kernel instance x (D + 2) words (acc, m, l);
     // fp32 for fixed chunks, 64-bit (value, epoch) for spans
@@ -218,7 +227,7 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
     const int per_launch = n_seqs < attn::kMaxSeqsPerLaunch ? n_seqs : attn::kMaxSeqsPerLaunch;
     plan->grid = 0;
     if (need_device) {
-        rc = resident_grid(pool, n_q_heads, plan->spans, &plan->grid);
+        rc = resident_grid(pool, n_q_heads, plan->spans, plan->cuda_cores, &plan->grid);
         if (rc) return rc;
     }
     // [reserved: 256 B][records][merge jobs]
@@ -227,7 +236,7 @@ int attention_plan(const pf_pool *pool, int n_seqs, int n_q_heads, int max_block
     if (plan->spans) {
         plan->chunk = TB;
         int grid = plan->grid;
-        if (!need_device && resident_grid(pool, n_q_heads, true, &grid) != PF_OK) {
+        if (!need_device && resident_grid(pool, n_q_heads, true, plan->cuda_cores, &grid) != PF_OK) {
             clear_error();
             grid = kGridBoundNoDevice;
         }
@@ -268,7 +277,7 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     KernelInfo ki;
     int HG = 0;
     bool mma = false;
-    int rc = kernel_for(pool, a.rows * pool->n_kv_heads, plan.spans, &ki, &HG, &mma);
+    int rc = kernel_for(pool, a.rows * pool->n_kv_heads, plan.spans, plan.cuda_cores, &ki, &HG, &mma);
     if (rc) return rc;
     int tmi = 0;
     rc = encode_pool_tmaps(pool, dev, mma ? 0 : HG, &tmi);
@@ -304,6 +313,12 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     p.prefetch_tiles = a.overlap_previous ? 16 : 6;
     p.gh = a.n_q_heads / pool->n_kv_heads;
     p.rows = a.rows;
+    p.wait_ns = kWaitLimitNs;
+    p.test_skip = 0;
+    if (g_inject_timeout.exchange(0) != 0) {
+        p.wait_ns = kInjectedWaitLimitNs;
+        p.test_skip = 1;
+    }
     const size_t out_elem = a.out_dtype == PF_F32 ? 4 : 2;
     const size_t row = (size_t)a.n_q_heads * pool->head_dim;   // q / out elements per sequence
 
@@ -372,3 +387,9 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
 }
 
 }  // namespace pkv
+
+extern "C" int pf_test_inject_wait_timeout(void) {
+    pkv::clear_error();
+    pkv::g_inject_timeout.store(1);
+    return PF_OK;
+}

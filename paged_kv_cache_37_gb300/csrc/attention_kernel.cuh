@@ -160,6 +160,10 @@ struct Params {
     const int32_t *cu_q;
     int gh;               // q-heads per kv-head
     int rows;             // rows per kv-head the call allows (gh for decode; <= the instance's G)
+    unsigned long long wait_ns;   // limit of every wait of the launch (kWaitLimitNs)
+    // Testing hook (0 normally): block 0 never fills its first ring stage,
+    // so the waits for it run out and the launch reports PF_DEV_WAIT_TIMEOUT.
+    int test_skip;
 };
 
 // Span map of the span schedule: the W flattened tiles cut into
@@ -535,8 +539,12 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     auto issue_stage = [&](int j0) -> bool {
         const int nsub = min(SUB, (it.ntok + TB - 1) / TB - j0);
         const int stage = st % NS;
-        if (!warp_wait(smem_addr(&sm.empty[stage]), ((st / NS) & 1) ^ 1, p.status, lane)) return false;
+        if (!warp_wait(smem_addr(&sm.empty[stage]), ((st / NS) & 1) ^ 1, p.status, lane, 0, p.wait_ns)) return false;
         const uint32_t full_bar = smem_addr(&sm.full[stage]);
+        if (p.test_skip && blockIdx.x == 0 && st == 0) {   // testing hook: nothing will fill this stage
+            ++st;
+            return true;
+        }
         if (B >= TB) {
             if (lane == 0) mbar_arrive_expect_tx(full_bar, (uint32_t)nsub * kTileBytes);
         }
@@ -604,7 +612,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
 
     for (int k = 0; ok; ++k) {
         const int slot = k % NQ;
-        if (!warp_wait(smem_addr(&sm.qempty[slot]), ((k / NQ) & 1) ^ 1, p.status, lane)) break;
+        if (!warp_wait(smem_addr(&sm.qempty[slot]), ((k / NQ) & 1) ^ 1, p.status, lane, 0, p.wait_ns)) break;
         if (it.done) {
             if (lane == 0) {
                 sm.desc[slot].s = -1;
@@ -679,11 +687,11 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     const uint32_t last = st < (uint32_t)NS ? st : (uint32_t)NS;
     for (uint32_t i = 0; i < last; ++i) {
         const uint32_t xs = st - 1 - i;
-        warp_wait(smem_addr(&sm.full[xs % NS]), (xs / NS) & 1, p.status, lane);
+        warp_wait(smem_addr(&sm.full[xs % NS]), (xs / NS) & 1, p.status, lane, 0, p.wait_ns);
     }
     for (int i = 0; i < NQ && i < posted; ++i) {
         const int xq = posted - 1 - i;
-        warp_wait(smem_addr(&sm.qfull[xq % NQ]), (xq / NQ) & 1, p.status, lane);
+        warp_wait(smem_addr(&sm.qfull[xq % NQ]), (xq / NQ) & 1, p.status, lane, 0, p.wait_ns);
     }
 }
 
@@ -944,7 +952,7 @@ __device__ __forceinline__ bool merge_span_pair(const Params &p, int first, int 
                     const unsigned long long now = global_timer_ns();
                     if (t_wait == 0) {
                         t_wait = now;
-                    } else if (now - t_wait > kWaitLimitNs) {
+                    } else if (now - t_wait > p.wait_ns) {
                         if (lane == 0) atomicOr(p.status, PF_DEV_WAIT_TIMEOUT);
                         return false;
                     }
@@ -1045,7 +1053,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
     int pending = 0;   // span schedule: bit c = this warp wrote a cut part's record in slot c
     for (int k = 0;; ++k) {
         const int slot = k % NQ;
-        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
+        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane, 0, p.wait_ns)) return;
         const ItemDesc d = sm.desc[slot];
         if (d.s < 0) {
             if (part == 0) merge_if_last<D, G, HG>(p, sm.pend[cw][0], pending, hl, lane);
@@ -1102,7 +1110,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
         const int ntiles = (d.ntok + TB - 1) / TB;
         for (int j = 0; j < ntiles; ++j, ++st) {
             const int stage = st % NS;
-            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane)) return;
+            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane, 0, p.wait_ns)) return;
             if (active) {
                 const __half *kt = sm.k[stage];
                 const __half *vt = sm.v[stage];
@@ -1222,7 +1230,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                     }
                 }
             }
-            if (!warps_sync(cbar, cphase, p.status, lane)) return;
+            if (!warps_sync(cbar, cphase, p.status, lane, p.wait_ns)) return;
             if (part == 0) {
 #pragma unroll
                 for (int g = 0; g < R; ++g) {
@@ -1249,7 +1257,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                     for (int i = 0; i < 8; ++i) acc[g][i] = a[i];
                 }
             }
-            if (!warps_sync(cbar, cphase, p.status, lane)) return;   // red[] is reused next item
+            if (!warps_sync(cbar, cphase, p.status, lane, p.wait_ns)) return;   // red[] is reused next item
         }
         const bool leader = (RSPLIT || part == 0) && active;
         if (d.kind == kWhole) {
@@ -1281,12 +1289,15 @@ __device__ __forceinline__ void store2(const Params &p, size_t o, float x0, floa
 // q-heads), HG kv-heads per item.  A head's rows (at most 16) form the M side
 // of warp-level tensor-core products, fp16 in, fp32 accumulate: scores
 // S = Q K^T over a 16-token tile (m16n8k16, two 8-token column blocks), then
-// O += P V with P the tile's weights rounded to fp16 (m16n8k16 per 8 dims).
-// The online softmax runs on the score fragments: lane (g, t) = (lane / 4,
-// lane % 4) holds rows g and g + 8, tokens 2t, 2t + 1 of each column block,
-// and the same rows of O at dims 8b + 2t, 8b + 2t + 1.  The weights' row sums
-// l are the sums of the rounded fp16 weights, so the normalised output is an
-// exact weighted mean of V under those weights.
+// O += P V (m16n8k16 per 8 dims).  The online softmax runs on the score
+// fragments: lane (g, t) = (lane / 4, lane % 4) holds rows g and g + 8,
+// tokens 2t, 2t + 1 of each column block, and the same rows of O at dims
+// 8b + 2t, 8b + 2t + 1.  fp16 output: P is the tile's weights rounded to
+// fp16 and the row sums l are the sums of those rounded weights, so the
+// normalised output is an exact weighted mean of V under them.  fp32 output:
+// P V is taken twice, with the weights' fp16 part and with its rounding
+// error (also fp16), and l sums the fp32 weights, so the weights keep about
+// 22 bits (the fp32-output path carries no fp16 rounding of the weights).
 //
 // Each head has WPH = NCW / HG consumer warps; its tiles are dealt
 // round-robin (warp part p computes tiles j = p mod WPH, whole).  With
@@ -1309,6 +1320,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
     const int part = cw % WPH;      // which of the head's tiles this warp computes
     const uint32_t hoff = (uint32_t)hl * (D / 64) * TB * 128;   // the head's bytes in a stage
     const int Hq = p.n_q_heads;
+    const bool hilo = p.out_f32 != 0;   // fp32 output: weights as fp16 hi + lo parts
 
     zero_empty_outputs<D>(p, cw, lane);
 
@@ -1318,7 +1330,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
     int pending = 0;   // span schedule: bit c = this warp wrote a cut part's record in slot c
     for (int k = 0;; ++k) {
         const int slot = k % NQ;
-        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
+        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane, 0, p.wait_ns)) return;
         const ItemDesc d = sm.desc[slot];
         if (d.s < 0) {
             merge_if_last<D, G, HG>(p, sm.pend[cw][0], pending, hl, lane);
@@ -1374,7 +1386,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
         const int ntiles = (d.ntok + TB - 1) / TB;
         for (int j0 = 0; j0 < ntiles; j0 += SUB, ++st) {
             const int stage = st % NS;
-            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane)) return;
+            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane, 0, p.wait_ns)) return;
             const int nsub = min(SUB, ntiles - j0);
             for (int u = 0; u < nsub; ++u) {
             const int j = j0 + u;   // tile of the item; the stage holds tile j at u * SUBH halves
@@ -1448,8 +1460,12 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                     }
                 }
                 // weights as the A fragment of P V: register 2 nb + r holds
-                // row g + 8 r, tokens 8 nb + 2t, 8 nb + 2t + 1
-                uint32_t pa[4];
+                // row g + 8 r, tokens 8 nb + 2t, 8 nb + 2t + 1.  fp16 output:
+                // the weights rounded to fp16, l their sum.  fp32 output: P
+                // = P_hi + P_lo, both fp16 (P_lo the rounding error of P_hi),
+                // and P V as two products, so the weights carry about 22
+                // bits; l sums the fp32 weights.
+                uint32_t pa[4], pl[4];
 #pragma unroll
                 for (int nb = 0; nb < 2; ++nb) {
 #pragma unroll
@@ -1459,8 +1475,14 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                         const float p1 = z1 == -INFINITY ? 0.0f : exp2f(z1 - m[r]);
                         const __half2 w = __floats2half2_rn(p0, p1);
                         const float2 wf = __half22float2(w);
-                        l[r] += wf.x + wf.y;
                         pa[2 * nb + r] = *reinterpret_cast<const uint32_t *>(&w);
+                        if (hilo) {
+                            const __half2 wl = __floats2half2_rn(p0 - wf.x, p1 - wf.y);
+                            pl[2 * nb + r] = *reinterpret_cast<const uint32_t *>(&wl);
+                            l[r] += p0 + p1;
+                        } else {
+                            l[r] += wf.x + wf.y;
+                        }
                     }
                 }
                 // O += P V: V rows (tokens) are the B fragments' k; one
@@ -1471,6 +1493,10 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                     ldmatrix_x4_trans(b, vb + swz((lane & 7) + ((lane >> 3) & 1) * 8, np * 2 + (lane >> 4)));
                     mma_f16_16816(o[2 * np], pa, b[0], b[1]);
                     mma_f16_16816(o[2 * np + 1], pa, b[2], b[3]);
+                    if (hilo) {
+                        mma_f16_16816(o[2 * np], pl, b[0], b[1]);
+                        mma_f16_16816(o[2 * np + 1], pl, b[2], b[3]);
+                    }
                 }
             }
             }
@@ -1500,7 +1526,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                     }
                 }
             }
-            if (!warps_sync(cbar, cphase, p.status, lane)) return;
+            if (!warps_sync(cbar, cphase, p.status, lane, p.wait_ns)) return;
             if (part == 0) {
                 const int w0 = hl * WPH;
 #pragma unroll
@@ -1535,7 +1561,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                     }
                 }
             }
-            if (!warps_sync(cbar, cphase, p.status, lane)) return;   // red[] is reused next item
+            if (!warps_sync(cbar, cphase, p.status, lane, p.wait_ns)) return;   // red[] is reused next item
         }
         if (part != 0 || !active) continue;
         if (d.kind == kWhole) {

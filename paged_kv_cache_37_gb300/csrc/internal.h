@@ -117,7 +117,8 @@ int launch_gather_kv(const GatherArgs &a, cudaStream_t stream);
 
 // How an attention call is scheduled and what workspace it needs.
 struct AttnPlan {
-    bool spans;            // balanced spans (split_tokens == 0) or fixed chunks
+    bool spans;            // balanced spans (split_tokens 0 or -2) or fixed chunks
+    bool cuda_cores;       // CUDA-core consumers (split_tokens != 0): fp32 scores and weights
     int chunk;             // chunk schedule: tokens per chunk
     int grid;              // persistent grid (0 when planned without a device)
     size_t counter_bytes;  // reserved bytes at the front of the workspace (256 B)

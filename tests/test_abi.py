@@ -144,4 +144,7 @@ def test_workspace_size_grows_with_split(pkv):
     auto = lib.pf_decode_workspace_bytes(pool, 128, 12, 128, 0)
     fine = lib.pf_decode_workspace_bytes(pool, 128, 12, 128, 16)
     assert 0 < never < auto < fine
+    # balanced spans on the CUDA cores: span records like the default schedule
+    assert never < lib.pf_decode_workspace_bytes(pool, 128, 12, 128, -2)
+    assert lib.pf_decode_workspace_bytes(pool, 128, 12, 128, -3) == 0
     lib.pf_pool_destroy(pool)
