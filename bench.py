@@ -65,6 +65,11 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--main-only", action="store_true",
                    help="time the decode step legs only (no side legs): the command profiles are taken with")
+    p.add_argument("--cpu-threads", type=int, default=0, help="host threads for the oracle (0: every core)")
+    p.add_argument("--record-traffic", metavar="RAW_CSV",
+                   help="write profiles/<--profile-name>.json from `ncu -i REP --page raw --csv` output, then exit")
+    p.add_argument("--profile-name", default="attention_mixed_shuffled")
+    p.add_argument("--profile-command", default="", help="the ncu command the capture came from (recorded)")
     return p.parse_args(argv)
 
 
@@ -157,21 +162,98 @@ def read_tensor_peak():
         return 1900.0, "fallback"
 
 
-def profile_traffic():
-    """dram bytes per attention launch from the committed ncu summary, or None
-    if the kernel source changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", "attention_mixed_shuffled.md")
+def profile_record(name):
+    """The JSON record that `--record-traffic` wrote from an ncu capture of the
+    decode kernel, or None if there is none or the kernel sources changed
+    since it was taken."""
+    path = os.path.join(ROOT, "profiles", name + ".json")
     try:
-        fields = {}
-        for line in open(path):
-            if ":" in line and line.startswith("- "):
-                k, v = line[2:].rsplit(":", 1)
-                fields[k.strip()] = v.strip().strip("`")
-        if fields.get("kernel sources sha256[:16]") != kernel_sources_hash():
-            return None
-        return int(fields["dram bytes per call"])
+        with open(path) as f:
+            rec = json.load(f)
+        return rec if rec.get("kernel_sources_sha16") == kernel_sources_hash() else None
     except Exception:
         return None
+
+
+def profile_traffic(name="attention_mixed_shuffled"):
+    """DRAM bytes (read + write) of one launch of the decode kernel in that
+    capture, or None."""
+    rec = profile_record(name)
+    return None if rec is None else int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+
+
+def profile_dram_summary():
+    """Per layout: DRAM bytes and the GB/s they make over the captured
+    launch's duration (ncu, one isolated launch: cold caches, serialised)."""
+    out = {}
+    for layout in ("shuffled", "ordered"):
+        rec = profile_record("attention_mixed_" + layout)
+        if rec and rec.get("duration_ns"):
+            b = int(rec["dram_bytes_read"]) + int(rec["dram_bytes_write"])
+            out[layout] = {"dram_bytes": b, "duration_us": rec["duration_ns"] / 1e3,
+                           "dram_gbs": round(b / rec["duration_ns"], 1)}
+    return out or None
+
+
+_UNITS = {"byte": 1, "b": 1, "kbyte": 1e3, "kb": 1e3, "mbyte": 1e6, "mb": 1e6, "gbyte": 1e9, "gb": 1e9,
+          "tbyte": 1e12, "tb": 1e12}
+_NS = {"nsecond": 1, "ns": 1, "usecond": 1e3, "us": 1e3, "msecond": 1e6, "ms": 1e6, "second": 1e9, "s": 1e9}
+
+
+def record_traffic(raw_csv, name, command):
+    """Read `ncu -i REP --page raw --csv` output (a header row of metric names,
+    a row of units, then one row per captured launch) and write the DRAM
+    bytes of the first decode-kernel launch to profiles/<name>.json."""
+    import csv
+    rows = list(csv.reader(open(raw_csv)))
+    head = next(i for i, r in enumerate(rows) if "dram__bytes_read.sum" in r)
+    names, units, data = rows[head], rows[head + 1], rows[head + 2:]
+    col = {n: i for i, n in enumerate(names)}
+    launch = next(r for r in data if "paged_decode" in r[col["Kernel Name"]])
+
+    def value(metric):
+        i = col[metric]
+        return int(round(float(launch[i].replace(",", "")) * _UNITS[units[i].strip().lower()]))
+
+    rec = {"kernel": launch[col["Kernel Name"]], "dram_bytes_read": value("dram__bytes_read.sum"),
+           "dram_bytes_write": value("dram__bytes_write.sum"),
+           "duration_ns": None, "kernel_sources_sha16": kernel_sources_hash(), "command": command}
+    if "gpu__time_duration.sum" in col:   # the raw page gives the duration in its own unit
+        i = col["gpu__time_duration.sum"]
+        scale = _NS[units[i].strip().lower()]
+        rec["duration_ns"] = int(round(float(launch[i].replace(",", "")) * scale))
+    out = os.path.join(ROOT, "profiles", name + ".json")
+    with open(out, "w") as f:
+        json.dump(rec, f, indent=1)
+        f.write("\n")
+    return out
+
+
+def host_cpu():
+    """(model name, logical cores this process may use) of the host."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith(("model name", "cpu model", "hardware")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except Exception:
+        cores = os.cpu_count() or 1
+    import platform
+    return f"{model or 'unknown'} ({platform.machine()})", cores
 
 
 def kernel_sources_hash():
@@ -253,11 +335,15 @@ def workload():
     return w, lens, maxb
 
 
-def oracle_step_timer(w, lens, bt, budget_s, max_steps=None):
+def oracle_step_timer(w, lens, bt, budget_s, max_steps=None, threads=0):
     """Run the fp64 oracle's decode step (scatter of the new tokens + paged
     attention) on host copies until budget_s has elapsed; returns (steps,
-    seconds, fraction of the workload per step)."""
+    seconds, threads).  The attention of a step is shared out over `threads`
+    host threads (0: every core this process may use) by sequence, each
+    thread calling the oracle on its own sequences (the C oracle runs
+    without the interpreter lock); the oracle itself is unchanged."""
     import oracle
+    from concurrent.futures import ThreadPoolExecutor
     oracle.build()
     S = len(lens)
     H, D, B, N = w["n_kv_heads"], w["head_dim"], w["block_size"], w["n_blocks"]
@@ -268,14 +354,28 @@ def oracle_step_timer(w, lens, bt, budget_s, max_steps=None):
     vn = si.fp16_normal((S, H, D), si.SEED_VALUES + 4)
     seq_idx = np.arange(S, dtype=np.int32)
     pos = (lens - 1).astype(np.int32)
+    n = threads or host_cpu()[1]
+    n = max(1, min(n, S))
+    # longest first onto the least-loaded thread: equal token counts per thread
+    load, parts = [0] * n, [[] for _ in range(n)]
+    for s in np.argsort(-lens, kind="stable"):
+        j = int(np.argmin(load))
+        parts[j].append(int(s))
+        load[j] += int(lens[s])
+    shares = [(q[np.array(p_)], bt[np.array(p_)], lens[np.array(p_)]) for p_ in parts if p_]
+
+    def attend(share):
+        oracle.attention_paged(share[0], k, v, 0, share[1], share[2], w["scale"])
+
     steps, t0 = 0, time.perf_counter()
-    while True:
-        oracle.scatter(k, v, 0, kn, vn, bt, seq_idx, pos)
-        oracle.attention_paged(q, k, v, 0, bt, lens, w["scale"])
-        steps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s or (max_steps and steps >= max_steps):
-            return steps, el
+    with ThreadPoolExecutor(max_workers=len(shares)) as ex:
+        while True:
+            oracle.scatter(k, v, 0, kn, vn, bt, seq_idx, pos)
+            list(ex.map(attend, shares))
+            steps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s or (max_steps and steps >= max_steps):
+                return steps, el, len(shares)
 
 
 # ----------------------------------------------------------------- ours
@@ -319,18 +419,23 @@ def run_ours(args, dist):
     sp = ctypes.c_void_p(stream.cuda_stream)
     P = lambda t: ctypes.c_void_p(t.data_ptr())
 
-    def arg_sets(layout, overlap=True):
+    def arg_sets(layout, overlap=True, split=None):
+        split = args.split if split is None else split
         bt = tables[layout]
-        ws_ = [(P(r["ws"]), r["ws"].numel()) for r in reps]
+        key = "ws" if split == args.split else f"ws{split}"
+        for r in reps:
+            if key not in r:
+                r[key] = pkv.make_workspace(r["pool"], S, Hq, maxb, split)
+        ws_ = [(P(r[key]), r[key].numel()) for r in reps]
         wr = [(r["pool"].handle, 0, P(r["kn"]), P(r["vn"]), P(bt), S, maxb, P(seq_d), P(pos_d), S, sp) for r in reps]
         at = [(r["pool"].handle, 0, P(r["q"]), P(bt), maxb, P(lens_d), S, Hq, ctypes.c_float(w["scale"]),
-               P(r["out"]), pkv.PF_F16, args.split, ws_[i][0], ws_[i][1], sp) for i, r in enumerate(reps)]
+               P(r["out"]), pkv.PF_F16, split, ws_[i][0], ws_[i][1], sp) for i, r in enumerate(reps)]
         # consecutive steps write neither the lengths nor the tables, so each
         # step's launch may overlap the previous step's kernel; a call timed
         # on its own (events around it) has nothing to overlap and does not ask
         flag = 0 if overlap is False else pkv.PF_STEP_OVERLAP_PREVIOUS
         fu = [(r["pool"].handle, 0, P(r["q"]), P(r["kn"]), P(r["vn"]), P(bt), maxb, P(lens_d), S, Hq,
-               ctypes.c_float(w["scale"]), P(r["out"]), pkv.PF_F16, args.split, ws_[i][0], ws_[i][1],
+               ctypes.c_float(w["scale"]), P(r["out"]), pkv.PF_F16, split, ws_[i][0], ws_[i][1],
                flag, sp)
               for i, r in enumerate(reps)]
         return wr, at, fu
@@ -339,8 +444,8 @@ def run_ours(args, dist):
         if rc:
             raise pkv.PagedKVError(rc, pkv.pf_last_error())
 
-    def run_steps(layout, n, events=None, fused=True):
-        wr, at, fu = arg_sets(layout, overlap=events is None)
+    def run_steps(layout, n, events=None, fused=True, split=None):
+        wr, at, fu = arg_sets(layout, overlap=events is None, split=split)
         for i in range(n):
             r = i % R
             if events is not None:
@@ -355,7 +460,7 @@ def run_ours(args, dist):
             if events is not None:
                 events[i][2].record(stream)
 
-    def timed(layout, n, with_events=False, fused=True):
+    def timed(layout, n, with_events=False, fused=True, split=None):
         evs = None
         if with_events:
             evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
@@ -363,7 +468,7 @@ def run_ours(args, dist):
         torch.cuda.synchronize(device)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        run_steps(layout, n, evs, fused)
+        run_steps(layout, n, evs, fused, split)
         e1.record(stream)
         torch.cuda.synchronize(device)
         dist.barrier()
@@ -400,6 +505,8 @@ def run_ours(args, dist):
     for fused in (True, False):
         run_steps("shuffled", W, fused=fused)
         run_steps("ordered", W, fused=fused)
+    for layout in ("shuffled", "ordered"):   # the CUDA-core consumers (split_tokens -2)
+        run_steps(layout, W, split=-2)
     torch.cuda.synchronize(device)
     pkv.pf_device_status(reset=True)
 
@@ -418,6 +525,14 @@ def run_ours(args, dist):
     ms_unf = dist.max(ms_unf)
     attn_ms = dist.max(per_unf["attn_ms"])
     write_ms = dist.max(per_unf["write_ms"])
+    # the same fused step on the CUDA-core consumers (balanced spans, fp32
+    # warp-shuffle dot products and weights, no tensor cores), both layouts
+    cc = {}
+    for layout in ("shuffled", "ordered"):
+        _, per_cc = timed(layout, K, with_events=True, split=-2)
+        cc[layout] = dist.max(per_cc["step_ms"])
+    ms_cc_b2b, _ = timed("shuffled", K, split=-2)
+    ms_cc_b2b = dist.max(ms_cc_b2b)
 
     # side legs (skipped with --main-only, e.g. under a profiler)
     peak, peak_src = read_peaks()
@@ -801,9 +916,20 @@ def run_ours(args, dist):
         "ordered": {"ms_per_step": round(ms_ord / K, 5), "decode_step_ms": round(step_ord_ms, 5),
                     "gbs": round(step_bytes / (step_ord_ms / 1e3) / 1e9, 1),
                     "shuffled_over_ordered_time": round(step_call_ms / step_ord_ms, 4)},
+        "cuda_cores": {"split_tokens": -2,
+                       "consumers": "warp-shuffle q.K over 8-lane groups, fp32 online softmax and weights, "
+                                    "no tensor cores (paged_decode_kernel_r128<64,1,4>)",
+                       "decode_step_ms": round(cc["shuffled"], 5),
+                       "gbs": round(step_bytes / (cc["shuffled"] / 1e3) / 1e9, 1),
+                       "frac_of_measured_copy": round(step_bytes / (cc["shuffled"] / 1e3) / 1e9 / peak, 4),
+                       "ordered_decode_step_ms": round(cc["ordered"], 5),
+                       "ordered_gbs": round(step_bytes / (cc["ordered"] / 1e3) / 1e9, 1),
+                       "shuffled_over_ordered_time": round(cc["shuffled"] / cc["ordered"], 4),
+                       "steps_back_to_back_ms": round(ms_cc_b2b / K, 5)},
         **side,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profile_traffic(),
+                     "ncu_dram": profile_dram_summary(),
                      "kernel": "pf_decode_step (paged_decode_kernel_mma_r128<64,1,4>: tensor-core consumers, fused write, "
                                "attention, in-kernel merge)",
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
@@ -813,11 +939,13 @@ def run_ours(args, dist):
         "clocks": clocks,
     }
     if dist.rank == 0:
-        steps_cpu, el = oracle_step_timer(w, lens, bt_shuf, args.cpu_budget_s)
-        res["cpu_baseline"] = {"value": round(step_bytes * steps_cpu / el / 1e9, 4), "unit": "GB/s", "cores": 1,
-                               "kind": "oracle",
+        steps_cpu, el, nthr = oracle_step_timer(w, lens, bt_shuf, args.cpu_budget_s, threads=args.cpu_threads)
+        model, ncores = host_cpu()
+        res["cpu_baseline"] = {"value": round(step_bytes * steps_cpu / el / 1e9, 4), "unit": "GB/s", "cores": nthr,
+                               "kind": "oracle", "cpu": model, "host_cores": ncores,
                                "sample": f"{steps_cpu} full decode steps of the same workload (scatter + fp64 "
-                                         f"two-pass attention) in {el:.1f} s, single thread"}
+                                         f"two-pass attention) in {el:.1f} s, the attention shared by sequence "
+                                         f"over {nthr} threads"}
     return res
 
 
@@ -835,24 +963,30 @@ def run_reference(args, dist):
     step_bytes = (attention_bytes(lens, w["n_q_heads"], w["n_kv_heads"], w["head_dim"], w["block_size"]) +
                   write_bytes(S, w["n_kv_heads"], w["head_dim"]))
     # warm-up steps (untimed), then timed steps, both capped
-    oracle_step_timer(w, lens, bt, 0.0, max_steps=max(1, min(args.warmup, 3)))
-    k_cap = max(1, min(args.steps, 30))
-    steps, el = oracle_step_timer(w, lens, bt, 1e9, max_steps=k_cap)
+    oracle_step_timer(w, lens, bt, 0.0, max_steps=max(1, min(args.warmup, 3)), threads=args.cpu_threads)
+    k_cap = max(1, min(args.steps, 100))
+    steps, el, nthr = oracle_step_timer(w, lens, bt, 1e9, max_steps=k_cap, threads=args.cpu_threads)
     value = step_bytes * steps / el / 1e9
-    sample = f"{steps} full decode steps (scatter + fp64 two-pass paged attention), single thread"
+    model, ncores = host_cpu()
+    sample = (f"{steps} full decode steps (scatter + fp64 two-pass paged attention), the attention shared by "
+              f"sequence over {nthr} threads")
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": args.gpus,
         "steps": steps, "warmup": args.warmup, "ms_per_step": round(el * 1e3 / steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, "split_tokens": args.split, "parallelism": "host, 1 thread"},
+        "config": {"workload": WORKLOAD_NAME, "split_tokens": args.split, "parallelism": f"host, {nthr} threads"},
         "tokens_per_s_per_layer": round(S * steps / el, 2),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": nthr, "kind": "oracle", "cpu": model,
+                         "host_cores": ncores, "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
 
 def main(argv=None):
     args = parse_args(argv)
+    if args.record_traffic:
+        print(record_traffic(args.record_traffic, args.profile_name, args.profile_command))
+        return
     dist = Dist()
     try:
         res = run_reference(args, dist) if args.impl == "reference" else run_ours(args, dist)

@@ -60,7 +60,12 @@ def test_reference_arm_prints_one_json_line():
     assert len(lines) == 1
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
-    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    import bench
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    # the oracle's attention is shared out over the host's cores (one thread
+    # per core, at most one per sequence), and the CPU model is recorded
+    assert d["cpu_baseline"]["cores"] == min(bench.host_cpu()[1], 128)
+    assert d["cpu_baseline"]["host_cores"] == bench.host_cpu()[1] and d["cpu_baseline"]["cpu"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
     assert d["metric"].startswith("paged decode-attention HBM GB/s")
 
@@ -73,3 +78,26 @@ def test_reference_arm_other_ranks_print_nothing():
     class Rank1:
         rank, world, local_rank = 1, 2, 1
     assert bench.run_reference(bench.parse_args(["--impl", "reference"]), Rank1()) is None
+
+
+def test_traffic_record_round_trip(tmp_path):
+    """--record-traffic reads ncu's raw page (metric names, a units row, one
+    row per launch) and the bench reads the bytes back, only while the kernel
+    sources are the ones the record names."""
+    import bench
+    raw = tmp_path / "raw.csv"
+    raw.write_text('"ID","Kernel Name","dram__bytes_read.sum","dram__bytes_write.sum","gpu__time_duration.sum"\n'
+                   '"","","Mbyte","Kbyte","usecond"\n'
+                   '"0","void attn::paged_decode_kernel_mma_r128<64, 1, 4>(...)","188.27","3,619.5","39.21"\n')
+    name = "test_traffic_tmp"
+    out = bench.record_traffic(str(raw), name, "ncu ...")
+    try:
+        rec = json.load(open(out))
+        assert rec["dram_bytes_read"] == 188270000 and rec["dram_bytes_write"] == 3619500
+        assert rec["duration_ns"] == 39210
+        assert bench.profile_traffic(name) == 188270000 + 3619500
+        rec["kernel_sources_sha16"] = "0" * 16
+        json.dump(rec, open(out, "w"))
+        assert bench.profile_traffic(name) is None
+    finally:
+        os.remove(out)
