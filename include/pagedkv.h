@@ -88,7 +88,9 @@ PF_API int pf_abi_version(void);
 /* ------------------------------------------------------------- pool ---- */
 
 /* Bytes of ONE of the two pools (K or V) for these dimensions; 0 if a
- * dimension is not positive or dtype is not PF_F16. */
+ * dimension is not positive or dtype is not PF_F16.  An implementation
+ * call with no counterpart on the pages: the size of the pool layout below,
+ * for the caller who allocates it. */
 PF_API size_t pf_pool_bytes(int n_layers, int n_blocks, int block_size,
                      int n_kv_heads, int head_dim, int dtype);
 
@@ -219,12 +221,16 @@ PF_API int pf_swap_in(const pf_pool *pool, const void *host_src,
 
 /* Workspace bytes pf_paged_decode_attention needs for a batch of n_seqs
  * sequences of at most max_blocks_per_seq * block_size tokens with
- * n_q_heads query heads and this split setting.  0 on bad arguments. */
+ * n_q_heads query heads and this split setting.  0 on bad arguments.  An
+ * implementation call with no counterpart on the pages (the workspace holds
+ * the partial results of split sequences, the reduction of the
+ * PagedAttention blog's "The Attention Kernel"). */
 PF_API size_t pf_decode_workspace_bytes(const pf_pool *pool, int n_seqs,
                                  int n_q_heads, int max_blocks_per_seq,
                                  int split_tokens);
 
-/* Prepare a workspace for first use (zero it).  Needed once after the
+/* Prepare a workspace for first use (zero it); an implementation call with
+ * no counterpart on the pages.  Needed once after the
  * workspace is allocated: everything a call reads back from the workspace
  * (merge jobs, the partial records of split sequences) carries a stamp of
  * the launch that wrote it, and zeroed memory holds no stamp of any launch.
@@ -377,17 +383,17 @@ PF_API int pf_paged_decode_attention_noalloc(const pf_pool *pool, int layer,
                                              int out_dtype, int split_tokens,
                                              void *stream);
 
-/* Testing hook for the bounded waits (no counterpart on the pages): the next
- * decode-attention launch in this process (pf_paged_decode_attention,
- * pf_decode_step, the noalloc variant, or the decode-kernel path of
- * pf_paged_prefill_attention) runs with a 2 ms wait limit instead of 1 s, and
- * its block 0 leaves the first stage of its copy ring unfilled.  The waits
- * for that stage, and the merge of any split sequence with a part in block
- * 0, give up after the limit: the kernel sets PF_DEV_WAIT_TIMEOUT, every
- * block returns (after its own copies in flight have landed), and the
- * context stays usable.  That launch's output is undefined; the next launch
- * with the same workspace computes normally.  Nothing is faulted and no
- * memory is touched out of bounds.  Always PF_OK. */
+/* Testing hook for the bounded waits (no counterpart on the pages): block 0
+ * of the next decode-attention launch in this process
+ * (pf_paged_decode_attention, pf_decode_step, the noalloc variant, or the
+ * decode-kernel path of pf_paged_prefill_attention) leaves the first stage of
+ * its copy ring unfilled.  Every wait in the library gives up after 1 s: the
+ * waits for that stage, and the merge of any split sequence with a part in
+ * block 0, run out (the launch takes a few seconds), the kernel sets
+ * PF_DEV_WAIT_TIMEOUT, every block returns (after its own copies in flight
+ * have landed), and the context stays usable.  That launch's output is
+ * undefined; the next launch with the same workspace computes normally.
+ * Nothing is faulted and no memory is touched out of bounds.  Always PF_OK. */
 PF_API int pf_test_inject_wait_timeout(void);
 
 /* Read the device status word (OR of pf_device_flag bits set by kernels of

@@ -445,9 +445,9 @@ def pf_paged_decode_attention_noalloc(pool, layer, q, block_tables, context_lens
 
 
 def pf_test_inject_wait_timeout():
-    """Testing hook: the next decode-attention launch leaves one stage of its
-    copy ring unfilled and waits 2 ms for it before giving up (see the C
-    header)."""
+    """Testing hook: block 0 of the next decode-attention launch leaves one
+    stage of its copy ring unfilled; the waits for it give up after 1 s (see
+    the C header)."""
     _check(lib().pf_test_inject_wait_timeout())
 
 

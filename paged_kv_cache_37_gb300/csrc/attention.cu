@@ -12,6 +12,7 @@
 namespace pkv {
 namespace {
 
+using attn::KernelFn;
 using attn::KernelInfo;
 using attn::TB;
 
@@ -170,8 +171,11 @@ int resident_grid(const pf_pool *pool, int n_q_heads, bool spans, bool cuda_core
     LaunchShape &sh = g_shapes[dev][D == 64 ? 0 : 1][G][HG][mma ? 1 : 0];
     if (!sh.ready) {
         const void *fn_ptr = reinterpret_cast<const void *>(ki.fn);
-        e = cudaFuncSetAttribute(fn_ptr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ki.smem);
-        if (e != cudaSuccess) return cuda_error(e, "attention: cudaFuncSetAttribute");
+        for (KernelFn f : {ki.fn, ki.fn32}) {   // fp16 and fp32 output instances
+            e = cudaFuncSetAttribute(reinterpret_cast<const void *>(f), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)ki.smem);
+            if (e != cudaSuccess) return cuda_error(e, "attention: cudaFuncSetAttribute");
+        }
         int occ = 0, sms = 0;
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn_ptr, attn::NTHREADS, ki.smem);
         if (e != cudaSuccess) return cuda_error(e, "attention: occupancy query");
@@ -197,10 +201,9 @@ unsigned next_epoch() {
 // Grid bound used to size span records when no device can be queried.
 constexpr int kGridBoundNoDevice = 4096;
 
-// pf_test_inject_wait_timeout: the next launch runs with a short wait limit
-// and block 0 leaves its first ring stage unfilled.
+// pf_test_inject_wait_timeout: block 0 of the next launch leaves its first
+// ring stage unfilled.
 std::atomic<int> g_inject_timeout{0};
-constexpr unsigned long long kInjectedWaitLimitNs = 2000000ull;   // 2 ms
 
 
 
@@ -313,12 +316,8 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     p.prefetch_tiles = a.overlap_previous ? 16 : 6;
     p.gh = a.n_q_heads / pool->n_kv_heads;
     p.rows = a.rows;
-    p.wait_ns = kWaitLimitNs;
-    p.test_skip = 0;
-    if (g_inject_timeout.exchange(0) != 0) {
-        p.wait_ns = kInjectedWaitLimitNs;
-        p.test_skip = 1;
-    }
+    p.test_skip = g_inject_timeout.exchange(0) != 0 ? 1 : 0;
+    const KernelFn fn = a.out_dtype == PF_F32 ? ki.fn32 : ki.fn;
     const size_t out_elem = a.out_dtype == PF_F32 ? 4 : 2;
     const size_t row = (size_t)a.n_q_heads * pool->head_dim;   // q / out elements per sequence
 
@@ -355,9 +354,9 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
             attr[0].val.programmaticStreamSerializationAllowed = 1;
             cfg.attrs = attr;
             cfg.numAttrs = 1;
-            e = cudaLaunchKernelEx(&cfg, ki.fn, pool->tmap_k[dev][tmi], pool->tmap_v[dev][tmi], p);
+            e = cudaLaunchKernelEx(&cfg, fn, pool->tmap_k[dev][tmi], pool->tmap_v[dev][tmi], p);
         } else {
-            ki.fn<<<plan.grid, attn::NTHREADS, ki.smem, stream>>>(pool->tmap_k[dev][tmi], pool->tmap_v[dev][tmi], p);
+            fn<<<plan.grid, attn::NTHREADS, ki.smem, stream>>>(pool->tmap_k[dev][tmi], pool->tmap_v[dev][tmi], p);
             e = cudaGetLastError();
         }
         if (e != cudaSuccess) return cuda_error(e, "pf_paged_decode_attention: launch");

@@ -9,9 +9,11 @@ namespace {
 template <int G, int HG>
 KernelInfo info() {
     if constexpr (RegisterCap<64, G, HG>::k128)
-        return {paged_decode_kernel_r128<64, G, HG>, sizeof(Smem<64, G, HG>), merge_kernel<64, G, HG>, G};
+        return {paged_decode_kernel_r128<64, G, HG>, sizeof(Smem<64, G, HG>), merge_kernel<64, G, HG>, G,
+                paged_decode_kernel_r128<64, G, HG>};
     else
-        return {paged_decode_kernel<64, G, HG>, sizeof(Smem<64, G, HG>), merge_kernel<64, G, HG>, G};
+        return {paged_decode_kernel<64, G, HG>, sizeof(Smem<64, G, HG>), merge_kernel<64, G, HG>, G,
+                paged_decode_kernel<64, G, HG>};
 }
 
 template <int HG>
@@ -25,7 +27,7 @@ KernelInfo by_group(int g) {
         case 6: return info<6, HG>();
         case 7: return info<7, HG>();
         case 8: return info<8, HG>();
-        default: return {nullptr, 0, nullptr, 0};
+        default: return {nullptr, 0, nullptr, 0, nullptr};
     }
 }
 
@@ -36,7 +38,7 @@ KernelInfo kernel_d64(int g, int hg) {
         case 1: return by_group<1>(g);
         case 2: return by_group<2>(g);
         case 4: return by_group<4>(g);
-        default: return {nullptr, 0, nullptr, 0};
+        default: return {nullptr, 0, nullptr, 0, nullptr};
     }
 }
 

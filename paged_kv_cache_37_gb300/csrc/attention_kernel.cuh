@@ -160,7 +160,6 @@ struct Params {
     const int32_t *cu_q;
     int gh;               // q-heads per kv-head
     int rows;             // rows per kv-head the call allows (gh for decode; <= the instance's G)
-    unsigned long long wait_ns;   // limit of every wait of the launch (kWaitLimitNs)
     // Testing hook (0 normally): block 0 never fills its first ring stage,
     // so the waits for it run out and the launch reports PF_DEV_WAIT_TIMEOUT.
     int test_skip;
@@ -539,9 +538,9 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     auto issue_stage = [&](int j0) -> bool {
         const int nsub = min(SUB, (it.ntok + TB - 1) / TB - j0);
         const int stage = st % NS;
-        if (!warp_wait(smem_addr(&sm.empty[stage]), ((st / NS) & 1) ^ 1, p.status, lane, 0, p.wait_ns)) return false;
+        if (!warp_wait(smem_addr(&sm.empty[stage]), ((st / NS) & 1) ^ 1, p.status, lane)) return false;
         const uint32_t full_bar = smem_addr(&sm.full[stage]);
-        if (p.test_skip && blockIdx.x == 0 && st == 0) {   // testing hook: nothing will fill this stage
+        if (st == 0 && p.test_skip && blockIdx.x == 0) {   // testing hook: nothing will fill this stage
             ++st;
             return true;
         }
@@ -612,7 +611,7 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
 
     for (int k = 0; ok; ++k) {
         const int slot = k % NQ;
-        if (!warp_wait(smem_addr(&sm.qempty[slot]), ((k / NQ) & 1) ^ 1, p.status, lane, 0, p.wait_ns)) break;
+        if (!warp_wait(smem_addr(&sm.qempty[slot]), ((k / NQ) & 1) ^ 1, p.status, lane)) break;
         if (it.done) {
             if (lane == 0) {
                 sm.desc[slot].s = -1;
@@ -687,11 +686,11 @@ __device__ __forceinline__ void producer(const CUtensorMap *tmk, const CUtensorM
     const uint32_t last = st < (uint32_t)NS ? st : (uint32_t)NS;
     for (uint32_t i = 0; i < last; ++i) {
         const uint32_t xs = st - 1 - i;
-        warp_wait(smem_addr(&sm.full[xs % NS]), (xs / NS) & 1, p.status, lane, 0, p.wait_ns);
+        warp_wait(smem_addr(&sm.full[xs % NS]), (xs / NS) & 1, p.status, lane);
     }
     for (int i = 0; i < NQ && i < posted; ++i) {
         const int xq = posted - 1 - i;
-        warp_wait(smem_addr(&sm.qfull[xq % NQ]), (xq / NQ) & 1, p.status, lane, 0, p.wait_ns);
+        warp_wait(smem_addr(&sm.qfull[xq % NQ]), (xq / NQ) & 1, p.status, lane);
     }
 }
 
@@ -952,7 +951,7 @@ __device__ __forceinline__ bool merge_span_pair(const Params &p, int first, int 
                     const unsigned long long now = global_timer_ns();
                     if (t_wait == 0) {
                         t_wait = now;
-                    } else if (now - t_wait > p.wait_ns) {
+                    } else if (now - t_wait > kWaitLimitNs) {
                         if (lane == 0) atomicOr(p.status, PF_DEV_WAIT_TIMEOUT);
                         return false;
                     }
@@ -1053,7 +1052,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
     int pending = 0;   // span schedule: bit c = this warp wrote a cut part's record in slot c
     for (int k = 0;; ++k) {
         const int slot = k % NQ;
-        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane, 0, p.wait_ns)) return;
+        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
         const ItemDesc d = sm.desc[slot];
         if (d.s < 0) {
             if (part == 0) merge_if_last<D, G, HG>(p, sm.pend[cw][0], pending, hl, lane);
@@ -1110,7 +1109,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
         const int ntiles = (d.ntok + TB - 1) / TB;
         for (int j = 0; j < ntiles; ++j, ++st) {
             const int stage = st % NS;
-            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane, 0, p.wait_ns)) return;
+            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane)) return;
             if (active) {
                 const __half *kt = sm.k[stage];
                 const __half *vt = sm.v[stage];
@@ -1230,7 +1229,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                     }
                 }
             }
-            if (!warps_sync(cbar, cphase, p.status, lane, p.wait_ns)) return;
+            if (!warps_sync(cbar, cphase, p.status, lane)) return;
             if (part == 0) {
 #pragma unroll
                 for (int g = 0; g < R; ++g) {
@@ -1257,7 +1256,7 @@ __device__ __forceinline__ void consumers(const Params &p, Smem<D, G, HG> &sm, i
                     for (int i = 0; i < 8; ++i) acc[g][i] = a[i];
                 }
             }
-            if (!warps_sync(cbar, cphase, p.status, lane, p.wait_ns)) return;   // red[] is reused next item
+            if (!warps_sync(cbar, cphase, p.status, lane)) return;   // red[] is reused next item
         }
         const bool leader = (RSPLIT || part == 0) && active;
         if (d.kind == kWhole) {
@@ -1303,7 +1302,7 @@ __device__ __forceinline__ void store2(const Params &p, size_t o, float x0, floa
 // round-robin (warp part p computes tiles j = p mod WPH, whole).  With
 // several warps per head their states meet in shared memory at the end and
 // the head's first warp carries the merged state on.
-template <int D, int G, int HG>
+template <int D, int G, int HG, bool HILO>
 __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, true> &sm, int cw, int lane) {
     constexpr int NS = Smem<D, G, HG, true>::NS;
     constexpr int SUB = Smem<D, G, HG, true>::SUB;   // tiles per stage
@@ -1320,7 +1319,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
     const int part = cw % WPH;      // which of the head's tiles this warp computes
     const uint32_t hoff = (uint32_t)hl * (D / 64) * TB * 128;   // the head's bytes in a stage
     const int Hq = p.n_q_heads;
-    const bool hilo = p.out_f32 != 0;   // fp32 output: weights as fp16 hi + lo parts
+    constexpr bool hilo = HILO;   // fp32 output: weights as fp16 hi + lo parts
 
     zero_empty_outputs<D>(p, cw, lane);
 
@@ -1330,7 +1329,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
     int pending = 0;   // span schedule: bit c = this warp wrote a cut part's record in slot c
     for (int k = 0;; ++k) {
         const int slot = k % NQ;
-        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane, 0, p.wait_ns)) return;
+        if (!warp_wait(smem_addr(&sm.qfull[slot]), (k / NQ) & 1, p.status, lane)) return;
         const ItemDesc d = sm.desc[slot];
         if (d.s < 0) {
             merge_if_last<D, G, HG>(p, sm.pend[cw][0], pending, hl, lane);
@@ -1386,7 +1385,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
         const int ntiles = (d.ntok + TB - 1) / TB;
         for (int j0 = 0; j0 < ntiles; j0 += SUB, ++st) {
             const int stage = st % NS;
-            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane, 0, p.wait_ns)) return;
+            if (!warp_wait(smem_addr(&sm.full[stage]), (st / NS) & 1, p.status, lane)) return;
             const int nsub = min(SUB, ntiles - j0);
             for (int u = 0; u < nsub; ++u) {
             const int j = j0 + u;   // tile of the item; the stage holds tile j at u * SUBH halves
@@ -1526,7 +1525,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                     }
                 }
             }
-            if (!warps_sync(cbar, cphase, p.status, lane, p.wait_ns)) return;
+            if (!warps_sync(cbar, cphase, p.status, lane)) return;
             if (part == 0) {
                 const int w0 = hl * WPH;
 #pragma unroll
@@ -1561,7 +1560,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
                     }
                 }
             }
-            if (!warps_sync(cbar, cphase, p.status, lane, p.wait_ns)) return;   // red[] is reused next item
+            if (!warps_sync(cbar, cphase, p.status, lane)) return;   // red[] is reused next item
         }
         if (part != 0 || !active) continue;
         if (d.kind == kWhole) {
@@ -1602,7 +1601,7 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
     }
 }
 
-template <int D, int G, int HG, bool MMA = false>
+template <int D, int G, int HG, bool MMA = false, bool HILO = false>
 __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const CUtensorMap &tmv, const Params &p) {
     using SM = Smem<D, G, HG, MMA>;
     constexpr int NS = SM::NS;
@@ -1692,7 +1691,7 @@ __device__ __forceinline__ void decode_attention(const CUtensorMap &tmk, const C
     }
     __syncthreads();
     if (warp == 0) producer<D, G, HG, MMA>(&tmk, &tmv, p, sm, lane);
-    else if constexpr (MMA) consumers_mma<D, G, HG>(p, sm, warp - 1, lane);
+    else if constexpr (MMA) consumers_mma<D, G, HG, HILO>(p, sm, warp - 1, lane);
     else consumers<D, G, HG>(p, sm, warp - 1, lane);
 }
 
@@ -1725,17 +1724,19 @@ __global__ void __maxnreg__(128) paged_decode_kernel_r128(const __grid_constant_
 // Tensor-core consumers, HG kv-heads per item (span schedule, block size
 // >= TB).  At head_dim 64 the state fits 128 registers (3 CTAs per SM); at
 // 128, 2 CTAs put up to 3 warps on a sub-partition: 168 registers.
-template <int D, int G, int HG>
+// HILO: the fp32-output instance (weights as fp16 hi + lo parts), a kernel
+// of its own so that the fp16 path's tile loop carries none of it.
+template <int D, int G, int HG, bool HILO>
 __global__ void __maxnreg__(168) paged_decode_kernel_mma(const __grid_constant__ CUtensorMap tmk,
                                                          const __grid_constant__ CUtensorMap tmv, const Params p) {
-    decode_attention<D, G, HG, true>(tmk, tmv, p);
+    decode_attention<D, G, HG, true, HILO>(tmk, tmv, p);
 }
 
-template <int D, int G, int HG>
+template <int D, int G, int HG, bool HILO>
 __global__ void __maxnreg__(128) paged_decode_kernel_mma_r128(const __grid_constant__ CUtensorMap tmk,
                                                               const __grid_constant__ CUtensorMap tmv,
                                                               const Params p) {
-    decode_attention<D, G, HG, true>(tmk, tmv, p);
+    decode_attention<D, G, HG, true, HILO>(tmk, tmv, p);
 }
 
 // Chunk schedule: merge the records of every job of this launch's epoch, one
@@ -1768,7 +1769,8 @@ struct KernelInfo {
     KernelFn fn;
     size_t smem;
     MergeFn merge;
-    int rows;   // rows per kv-head of the instance (its G): the size of a record's rows
+    int rows;      // rows per kv-head of the instance (its G): the size of a record's rows
+    KernelFn fn32; // the instance for fp32 output (the same as fn except on the tensor-core path)
 };
 
 // Defined in attention_d64.cu / attention_d128.cu / attention_mma.cu (the
@@ -1788,8 +1790,9 @@ KernelInfo mma_info() {
     constexpr size_t smem = sizeof(Smem<D, G, HG, true>) + 1024;
     // with the 1 KB each CTA reserves: 3 CTAs per SM (228 KB) at head_dim 64, 2 at 128
     static_assert(smem + 1024 <= (D == 64 ? 228 * 1024 / 3 : 228 * 1024 / 2), "shared memory per CTA");
-    if constexpr (D == 64) return {paged_decode_kernel_mma_r128<D, G, HG>, smem, nullptr, G};
-    else return {paged_decode_kernel_mma<D, G, HG>, smem, nullptr, G};
+    if constexpr (D == 64)
+        return {paged_decode_kernel_mma_r128<D, G, HG, false>, smem, nullptr, G, paged_decode_kernel_mma_r128<D, G, HG, true>};
+    else return {paged_decode_kernel_mma<D, G, HG, false>, smem, nullptr, G, paged_decode_kernel_mma<D, G, HG, true>};
 }
 
 template <int D, int G>
@@ -1799,8 +1802,8 @@ KernelInfo mma_by_heads(int hg) {
         case 2: return mma_info<D, G, 2>();
         case 4:
             if constexpr (D == 64 || G <= 8) return mma_info<D, G, 4>();
-            else return {nullptr, 0, nullptr, 0};
-        default: return {nullptr, 0, nullptr, 0};
+            else return {nullptr, 0, nullptr, 0, nullptr};
+        default: return {nullptr, 0, nullptr, 0, nullptr};
     }
 }
 

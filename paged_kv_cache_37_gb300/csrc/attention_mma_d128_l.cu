@@ -9,7 +9,7 @@ namespace attn {
 KernelInfo kernel_mma_d128_l(int g, int hg) {
     if (g <= 12) return mma_by_heads<128, 12>(hg);
     if (g <= 16) return mma_by_heads<128, 16>(hg);
-    return {nullptr, 0, nullptr, 0};
+    return {nullptr, 0, nullptr, 0, nullptr};
 }
 
 }  // namespace attn

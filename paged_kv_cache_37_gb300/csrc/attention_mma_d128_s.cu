@@ -10,7 +10,7 @@ KernelInfo kernel_mma_d128_s(int g, int hg) {
     if (g <= 1) return mma_by_heads<128, 1>(hg);
     if (g <= 4) return mma_by_heads<128, 4>(hg);
     if (g <= 8) return mma_by_heads<128, 8>(hg);
-    return {nullptr, 0, nullptr, 0};
+    return {nullptr, 0, nullptr, 0, nullptr};
 }
 
 }  // namespace attn

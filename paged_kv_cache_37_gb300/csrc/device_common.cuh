@@ -66,16 +66,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Wait until the phase with the given parity has completed.  Bounded: after
-// limit_ns it ORs PF_DEV_WAIT_TIMEOUT into *status and returns false.
+// kWaitLimitNs it ORs PF_DEV_WAIT_TIMEOUT into *status and returns false.
 // sleep_ns > 0 backs off between polls (for waits off the critical path).
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status, uint32_t sleep_ns = 0,
-                                          unsigned long long limit_ns = kWaitLimitNs) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *status, uint32_t sleep_ns = 0) {
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = global_timer_ns();
     for (uint32_t i = 1;; ++i) {
         if (sleep_ns) __nanosleep(sleep_ns);
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_timer_ns() - t0 > limit_ns) {
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
             atomicOr(status, PF_DEV_WAIT_TIMEOUT);
             return false;
         }
@@ -85,20 +84,19 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int *st
 // Warp-uniform bounded wait: lane 0 polls, the result is broadcast, and the
 // __shfl_sync orders the other lanes' later shared-memory reads after it.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int *status, int lane,
-                                          uint32_t sleep_ns = 0, unsigned long long limit_ns = kWaitLimitNs) {
+                                          uint32_t sleep_ns = 0) {
     int ok = 1;
-    if (lane == 0) ok = mbar_wait(bar, parity, status, sleep_ns, limit_ns) ? 1 : 0;
+    if (lane == 0) ok = mbar_wait(bar, parity, status, sleep_ns) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
 // Barrier among `count` warps built on an mbarrier initialised with that
 // count: each warp's lane 0 arrives after the warp's writes, then waits
 // (bounded) for the phase.  `phase` counts this barrier's uses.
-__device__ __forceinline__ bool warps_sync(uint32_t bar, uint32_t &phase, int *status, int lane,
-                                           unsigned long long limit_ns = kWaitLimitNs) {
+__device__ __forceinline__ bool warps_sync(uint32_t bar, uint32_t &phase, int *status, int lane) {
     __syncwarp();
     if (lane == 0) mbar_arrive(bar);
-    const bool ok = warp_wait(bar, phase & 1u, status, lane, 0, limit_ns);
+    const bool ok = warp_wait(bar, phase & 1u, status, lane);
     ++phase;
     return ok;
 }

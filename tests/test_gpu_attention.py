@@ -319,9 +319,9 @@ def test_peaked_softmax_long_contexts(pkv, cuda_dev, oracle_mod, split):
 def test_wait_that_runs_out_reports_and_recovers(pkv, cuda_dev, oracle_mod, split):
     """The bounded waits, made to run out on purpose: the testing hook makes
     block 0 leave one stage of its copy ring unfilled (a barrier that nothing
-    completes) under a 2 ms wait limit.  The launch must come back with
-    PF_DEV_WAIT_TIMEOUT and a usable context, and the next call on the same
-    workspace must match the oracle again (partial records carry their
+    completes); every wait gives up after 1 s.  The launch must come back
+    with PF_DEV_WAIT_TIMEOUT and a usable context, and the next call on the
+    same workspace must match the oracle again (partial records carry their
     launch's stamp, so nothing the timed-out launch left behind is read)."""
     w = si.WORKLOADS["mixed"]
     lens = si.band_lengths(w["bands"])
