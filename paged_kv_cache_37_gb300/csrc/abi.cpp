@@ -92,7 +92,7 @@ int pf_pool_create(pf_pool **out, void *k_base, void *v_base, int n_layers, int 
     p->head_dim = head_dim;
     p->dtype = dtype;
     for (int i = 0; i < pkv::kMaxDevices; ++i)
-        for (int j = 0; j < 4; ++j) p->tmap_ready[i][j] = false;
+        for (int j = 0; j < 6; ++j) p->tmap_ready[i][j] = false;
     *out = p;
     return PF_OK;
 }

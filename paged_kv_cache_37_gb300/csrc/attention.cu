@@ -84,10 +84,13 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     return fn;
 }
 
-// hg > 0: boxes {D, hg heads, TB rows}, unswizzled.  hg == 0: the
-// tensor-core layout, one head, 64-element halves of a row swizzled in
-// 128-byte rows: {64, TB} boxes of a 3-D map at head_dim 64, of a 4-D map
-// {64, D / 64, heads, rows} at head_dim 128.
+// hg > 0: boxes {D, hg heads, TB rows}, unswizzled.  hg < 0: the
+// tensor-core layout for -hg kv-heads, 64-element halves of a row swizzled
+// in 128-byte rows, one box per tile with the heads outermost: the map's
+// dimensions are ordered (64 elements, rows, heads) at head_dim 64 and (64,
+// rows, halves, heads) at 128 (strides need not grow with the dimension), so
+// a box {64, TB, (2,) -hg} lands as [head][half][row][64] -- each head's
+// 16-row, 128-byte-row blocks contiguous, swizzled by row mod 8.
 int encode_one(CUtensorMap *map, void *base, const pf_pool *pool, int hg) {
     auto encode = get_encode_fn();
     if (!encode) return set_error(PF_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
@@ -97,17 +100,24 @@ int encode_one(CUtensorMap *map, void *base, const pf_pool *pool, int hg) {
     const int box_rows = pool->block_size < TB ? pool->block_size : TB;
     cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
     CUresult r;
-    if (hg > 0 || D == 64) {
+    if (hg > 0) {
         cuuint64_t dims[3] = {D, H, (cuuint64_t)rows};
         cuuint64_t strides[2] = {D * 2, H * D * 2};
-        cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)(hg > 0 ? hg : 1), (cuuint32_t)box_rows};
+        cuuint32_t box[3] = {(cuuint32_t)D, (cuuint32_t)hg, (cuuint32_t)box_rows};
         r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, hg > 0 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else if (D == 64) {
+        cuuint64_t dims[3] = {64, (cuuint64_t)rows, H};
+        cuuint64_t strides[2] = {H * D * 2, D * 2};
+        cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, (cuuint32_t)(-hg)};
+        r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, base, dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     } else {
-        cuuint64_t dims[4] = {64, D / 64, H, (cuuint64_t)rows};
-        cuuint64_t strides[3] = {128, D * 2, H * D * 2};
-        cuuint32_t box[4] = {64u, 1u, 1u, (cuuint32_t)box_rows};
+        cuuint64_t dims[4] = {64, (cuuint64_t)rows, D / 64, H};
+        cuuint64_t strides[3] = {H * D * 2, 128, D * 2};
+        cuuint32_t box[4] = {64u, (cuuint32_t)box_rows, (cuuint32_t)(D / 64), (cuuint32_t)(-hg)};
         r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, base, dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -120,7 +130,8 @@ int encode_one(CUtensorMap *map, void *base, const pf_pool *pool, int hg) {
 }  // namespace
 
 int encode_pool_tmaps(pf_pool *pool, int device, int hg, int *index) {
-    const int i = hg == 0 ? 3 : (hg == 1 ? 0 : (hg == 2 ? 1 : 2));
+    const int a = hg < 0 ? -hg : hg;
+    const int i = (hg < 0 ? 3 : 0) + (a == 1 ? 0 : (a == 2 ? 1 : 2));
     *index = i;
     std::lock_guard<std::mutex> lock(pool->mu);
     if (pool->tmap_ready[device][i]) return PF_OK;
@@ -283,7 +294,7 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     int rc = kernel_for(pool, a.rows * pool->n_kv_heads, plan.spans, plan.cuda_cores, &ki, &HG, &mma);
     if (rc) return rc;
     int tmi = 0;
-    rc = encode_pool_tmaps(pool, dev, mma ? 0 : HG, &tmi);
+    rc = encode_pool_tmaps(pool, dev, mma ? -HG : HG, &tmi);
     if (rc) return rc;
 
     attn::Params p;
@@ -306,14 +317,14 @@ int launch_attention(const AttnArgs &a, cudaStream_t stream) {
     p.spans = plan.spans ? 1 : 0;
     p.out_f32 = a.out_dtype == PF_F32;
     p.scale_log2 = a.scale * 1.4426950408889634f;
-    // L2 prefetch of each CTA's first tiles before the dependency wait.
-    // Measured on the mixed workload: back to back (the launch overlaps the
-    // previous kernel's tail), 4 tiles 42.75 us, 8: 41.9, 16: 41.5, 20: 42.0,
-    // 24: 43.3 (16 tiles per CTA x 456 CTAs is about the size of L2); a call
-    // on its own, 0 tiles 42.0-42.9 us, 2: 41.9-42.0, 4: 41.4-41.6, 6:
-    // 41.2, 8: 41.3-41.5, 12: 42.8.  The prefetches reach DRAM ahead of the
-    // ring's loads, which then find their lines on the way in.
-    p.prefetch_tiles = a.overlap_previous ? 16 : 6;
+    // L2 prefetch of each CTA's first tiles before the dependency wait (one
+    // TMA prefetch per K or V tile).  Measured on the mixed workload: back to
+    // back (the launch overlaps the previous kernel's tail), 16 tiles 32.56
+    // us, 20: 32.63, 24: 32.43, 32: 32.88; a call on its own, 6 tiles 39.1 us,
+    // 8: 39.4, 10: 40.2, 16: 42.7 (and 0 tiles 0.5-1 us slower than 6).  The
+    // prefetches reach DRAM ahead of the ring's loads, which then find their
+    // lines on the way in.
+    p.prefetch_tiles = a.overlap_previous ? 24 : 6;
     p.gh = a.n_q_heads / pool->n_kv_heads;
     p.rows = a.rows;
     p.test_skip = g_inject_timeout.exchange(0) != 0 ? 1 : 0;

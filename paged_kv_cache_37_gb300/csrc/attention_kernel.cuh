@@ -305,42 +305,22 @@ __device__ __forceinline__ uint32_t swz(int t, int c) {
 }
 
 // Issue one K or V tile (pool rows r .. r + TB - 1 of heads h0 ..) into a
-// stage.  Plain: one box {D, HG, TB}.  MMA: per head and 64-element half of
-// the head, one swizzled box {64, TB} to stage offset (head * D / 64 + half)
-// * TB * 64; the boxes of a token's heads are issued back to back, so a page
-// row is still read as one run.
+// stage.  Plain: one box {D, HG, TB}.  MMA: one swizzled box {64, TB, (D /
+// 64,) HG} of the heads-outermost map, landing as [head][half][row][64]:
+// head hl's half hf at stage offset (hl * D / 64 + hf) * TB * 64.
 template <int D, int HG, bool MMA>
 __device__ __forceinline__ void tile_load(__half *dst, const CUtensorMap *map, int h0, int r, uint32_t bar,
                                           uint64_t pol) {
-    if constexpr (!MMA) {
-        tma_load_3d(smem_addr(dst), map, 0, h0, r, bar, pol);
-    } else {
-#pragma unroll
-        for (int hl = 0; hl < HG; ++hl) {
-#pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf) {
-                const uint32_t a = smem_addr(dst + (hl * (D / 64) + hf) * TB * 64);
-                if constexpr (D == 64) tma_load_3d(a, map, 0, h0 + hl, r, bar, pol);
-                else tma_load_4d(a, map, 0, hf, h0 + hl, r, bar, pol);
-            }
-        }
-    }
+    if constexpr (!MMA) tma_load_3d(smem_addr(dst), map, 0, h0, r, bar, pol);
+    else if constexpr (D == 64) tma_load_3d(smem_addr(dst), map, 0, r, h0, bar, pol);
+    else tma_load_4d(smem_addr(dst), map, 0, r, 0, h0, bar, pol);
 }
 
 template <int D, int HG, bool MMA>
 __device__ __forceinline__ void tile_prefetch(const CUtensorMap *map, int h0, int r) {
-    if constexpr (!MMA) {
-        tma_prefetch_3d(map, 0, h0, r);
-    } else {
-#pragma unroll
-        for (int hl = 0; hl < HG; ++hl) {
-#pragma unroll
-            for (int hf = 0; hf < D / 64; ++hf) {
-                if constexpr (D == 64) tma_prefetch_3d(map, 0, h0 + hl, r);
-                else tma_prefetch_4d(map, 0, hf, h0 + hl, r);
-            }
-        }
-    }
+    if constexpr (!MMA) tma_prefetch_3d(map, 0, h0, r);
+    else if constexpr (D == 64) tma_prefetch_3d(map, 0, r, h0);
+    else tma_prefetch_4d(map, 0, r, 0, h0);
 }
 
 template <int D, int G, int HG, bool MMA = false>

@@ -42,9 +42,11 @@ struct pf_pool {
     std::mutex mu;
     // [device][0, 1, 2: boxes of 1, 2, 4 kv-heads; 3: the tensor-core
     // layout (one kv-head, swizzled 64-element halves)]
-    bool tmap_ready[pkv::kMaxDevices][4];
-    CUtensorMap tmap_k[pkv::kMaxDevices][4];
-    CUtensorMap tmap_v[pkv::kMaxDevices][4];
+    // per device: boxes of 1, 2, 4 kv-heads (CUDA-core consumers), then the
+    // tensor-core layout for 1, 2, 4 kv-heads per item
+    bool tmap_ready[pkv::kMaxDevices][6];
+    CUtensorMap tmap_k[pkv::kMaxDevices][6];
+    CUtensorMap tmap_v[pkv::kMaxDevices][6];
 };
 
 namespace pkv {
