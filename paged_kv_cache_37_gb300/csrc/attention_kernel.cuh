@@ -109,7 +109,7 @@ struct PendPart {
     int s, h0, first, z_first, n_parts, qrow0, nq;
 };
 
-constexpr int kMaxSeqsPerLaunch = 1024;
+constexpr int kMaxSeqsPerLaunch = 512;
 
 // Span schedule: a (sequence, head-group) pair costs its tiles plus
 // kPairCost "cost units" (tiles' worth) in the partition, so spans of many
@@ -216,7 +216,8 @@ struct MmaShape {
     static constexpr int TILE_BYTES = 2 * TB * HG * D * 2;   // K and V of one tile
     static constexpr int BUDGET = (D == 64 ? 228 * 1024 / 3 : 228 * 1024 / 2) - 2048;   // reserved + alignment slack
     static constexpr bool MERGE = NCW / HG > 1;   // several warps per head meet in shared memory
-    static constexpr int FIXED = NQ * HG * G * D * 2 + NQ * 2 * HG * D * 2 + (MERGE ? NCW : 1) * G * (D + 2) * 4 +
+    static constexpr int REDW = MERGE ? HG * (NCW / HG - 1) : 1;   // merge slots: a head's warps but its first
+    static constexpr int FIXED = NQ * HG * G * D * 2 + NQ * 2 * HG * D * 2 + REDW * G * (D + 2) * 4 +
                                  (kMaxSeqsPerLaunch + 1) * 4 + kMaxSeqsPerLaunch + 1024;   // + barriers, items
     static constexpr int SUB_WANT = TILE_BYTES >= kMmaStageMinBytes ? 1 : kMmaStageMinBytes / TILE_BYTES;
     static constexpr int SUB_FIT = (BUDGET - FIXED) / (2 * TILE_BYTES);   // at least two stages
@@ -237,7 +238,9 @@ struct __align__(128) Smem {
     __half v[NS][SUB * Shape<D, HG>::STAGE_HALVES];
     __half q[NQ][HG * G * D];
     __half knew[NQ][2][HG * D];   // fused step: the new token's K and V rows of the item's heads
-    float red[(MMA ? MmaShape<D, G, HG>::MERGE : Shape<D, HG>::WPH > 1) ? NCW : 1][G][D + 2];   // per consumer warp: acc[D], m, l
+    // acc[D], m, l per merging warp: every consumer warp (CUDA cores), a head's
+    // warps but its first (tensor cores)
+    float red[MMA ? MmaShape<D, G, HG>::REDW : (Shape<D, HG>::WPH > 1 ? NCW : 1)][G][D + 2];
     ItemDesc desc[NQ];
     uint64_t full[NS];
     uint64_t empty[NS];
@@ -1489,44 +1492,51 @@ __device__ __forceinline__ void consumers_mma(const Params &p, Smem<D, G, HG, tr
         }
 
         if (WPH > 1 && ntiles > 1) {
-            // The head's warps' states meet in shared memory (rows < G); its
-            // first warp merges them with the log-sum-exp rule.
+            // The head's warps' states meet in shared memory (rows < G): its
+            // other warps leave theirs there, and its first warp merges them
+            // into its own with the log-sum-exp rule.
+            const int w1 = hl * (WPH - 1);   // the head's merge slots
+            if (part != 0) {
 #pragma unroll
-            for (int r = 0; r < 2; ++r) {
-                const int g = gq + 8 * r;
-                if (g < G) {
-                    float *rw = sm.red[cw][g];
+                for (int r = 0; r < 2; ++r) {
+                    const int g = gq + 8 * r;
+                    if (g < G) {
+                        float *rw = sm.red[w1 + part - 1][g];
 #pragma unroll
-                    for (int b = 0; b < NNB; ++b)
-                        *reinterpret_cast<float2 *>(rw + b * 8 + 2 * tq) = make_float2(o[b][2 * r], o[b][2 * r + 1]);
-                    if (tq == 0) {
-                        rw[D] = m[r];
-                        rw[D + 1] = l[r];
+                        for (int b = 0; b < NNB; ++b)
+                            *reinterpret_cast<float2 *>(rw + b * 8 + 2 * tq) = make_float2(o[b][2 * r], o[b][2 * r + 1]);
+                        if (tq == 0) {
+                            rw[D] = m[r];
+                            rw[D + 1] = l[r];
+                        }
                     }
                 }
             }
             if (!warps_sync(cbar, cphase, p.status, lane)) return;
             if (part == 0) {
-                const int w0 = hl * WPH;
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
                     const int g = gq + 8 * r;
                     if (g >= G) continue;
-                    float mx = -INFINITY;
+                    float mx = m[r];
 #pragma unroll
-                    for (int w = 0; w < WPH; ++w) mx = fmaxf(mx, sm.red[w0 + w][g][D]);
-                    float ls = 0.0f;
+                    for (int w = 1; w < WPH; ++w) mx = fmaxf(mx, sm.red[w1 + w - 1][g][D]);
+                    const float f0 = m[r] == -INFINITY ? 0.0f : exp2f(m[r] - mx);
+                    float ls = l[r] * f0;
                     float a[NNB][2];
 #pragma unroll
-                    for (int b = 0; b < NNB; ++b) a[b][0] = a[b][1] = 0.0f;
+                    for (int b = 0; b < NNB; ++b) {
+                        a[b][0] = o[b][2 * r] * f0;
+                        a[b][1] = o[b][2 * r + 1] * f0;
+                    }
 #pragma unroll
-                    for (int w = 0; w < WPH; ++w) {
-                        const float mw = sm.red[w0 + w][g][D];
+                    for (int w = 1; w < WPH; ++w) {
+                        const float mw = sm.red[w1 + w - 1][g][D];
                         const float f = mw == -INFINITY ? 0.0f : exp2f(mw - mx);
-                        ls = fmaf(sm.red[w0 + w][g][D + 1], f, ls);
+                        ls = fmaf(sm.red[w1 + w - 1][g][D + 1], f, ls);
 #pragma unroll
                         for (int b = 0; b < NNB; ++b) {
-                            const float2 v = *reinterpret_cast<const float2 *>(&sm.red[w0 + w][g][b * 8 + 2 * tq]);
+                            const float2 v = *reinterpret_cast<const float2 *>(&sm.red[w1 + w - 1][g][b * 8 + 2 * tq]);
                             a[b][0] = fmaf(v.x, f, a[b][0]);
                             a[b][1] = fmaf(v.y, f, a[b][1]);
                         }
