@@ -91,8 +91,10 @@ int pf_pool_create(pf_pool **out, void *k_base, void *v_base, int n_layers, int 
     p->n_kv_heads = n_kv_heads;
     p->head_dim = head_dim;
     p->dtype = dtype;
-    for (int i = 0; i < pkv::kMaxDevices; ++i)
+    for (int i = 0; i < pkv::kMaxDevices; ++i) {
         for (int j = 0; j < 6; ++j) p->tmap_ready[i][j] = false;
+        p->tmap_pf_ready[i] = false;
+    }
     *out = p;
     return PF_OK;
 }

@@ -25,6 +25,11 @@ constexpr int kMaxDevices = 64;
 // Tile height (tokens) the attention kernel stages per TMA transaction.
 constexpr int kTileTokens = 16;
 
+// pf_paged_prefill_attention without the decode kernel: at least this many
+// query rows (new tokens x q-heads per kv-head) per (sequence, kv-head) take
+// the tcgen05 kernel, fewer the warp-level MMA kernel.
+constexpr int kTcMinRows = 128;
+
 }  // namespace pkv
 
 // Non-owning description of caller-owned K and V pools.
@@ -40,13 +45,16 @@ struct pf_pool {
     // TMA descriptors over K and V viewed as [rows][n_kv_heads][head_dim]
     // with rows = n_layers * n_blocks * block_size, encoded lazily per device.
     std::mutex mu;
-    // [device][0, 1, 2: boxes of 1, 2, 4 kv-heads; 3: the tensor-core
-    // layout (one kv-head, swizzled 64-element halves)]
     // per device: boxes of 1, 2, 4 kv-heads (CUDA-core consumers), then the
     // tensor-core layout for 1, 2, 4 kv-heads per item
     bool tmap_ready[pkv::kMaxDevices][6];
     CUtensorMap tmap_k[pkv::kMaxDevices][6];
     CUtensorMap tmap_v[pkv::kMaxDevices][6];
+    // per device: the prompt kernel's boxes (one 64-element half of up to a
+    // page of rows of one kv-head, swizzled)
+    bool tmap_pf_ready[pkv::kMaxDevices];
+    CUtensorMap tmap_pf_k[pkv::kMaxDevices];
+    CUtensorMap tmap_pf_v[pkv::kMaxDevices];
 };
 
 namespace pkv {
@@ -103,6 +111,7 @@ struct PrefillArgs {
     int out_dtype;
 };
 int launch_prefill(const PrefillArgs &a, cudaStream_t stream);   // prefill_mma.cu
+int launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);   // prefill_tc.cu
 
 struct GatherArgs {
     const pf_pool *pool;

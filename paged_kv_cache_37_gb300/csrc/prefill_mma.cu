@@ -353,6 +353,8 @@ int launch_prefill(const PrefillArgs &a, cudaStream_t stream) {
     if (a.n_seqs > 65535 || pool->n_kv_heads > 65535)
         return set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: at most 65535 sequences and kv-heads per call");
     const int gh = a.n_q_heads / pool->n_kv_heads;
+    // 128 rows or more per (sequence, kv-head): the tcgen05 kernel
+    if ((long long)a.max_new * gh >= kTcMinRows) return launch_prefill_tc(a, stream);
     const long long n_qt = ((long long)a.max_new * gh + prefill_mma::QR - 1) / prefill_mma::QR;
     if (n_qt > 0x7fffffffll)
         return set_error(PF_ERR_INVALID, "pf_paged_prefill_attention: too many new tokens for one launch");
