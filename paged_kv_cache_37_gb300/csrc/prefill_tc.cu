@@ -15,19 +15,24 @@
 //                      of its tile, which is lane t of tensor memory;
 //   warp 8             the loader: K and V tiles of BN tokens (128 at
 //                      head_dim 64, 64 at 128) through the block table into
-//                      a ring of three stages, by TMA boxes of whole pages
+//                      a ring of four stages, by TMA boxes of whole pages
 //                      (block size 16 and up) or 16-byte cp.async per token
 //                      (block size 1), in the 128-byte swizzled layout;
 //   warp 9             owns the tensor memory; its lane 0 issues the MMAs.
 // Per K/V tile j and query tile g the MMA warp computes S_g = Q_g K_j^T into
 // tensor memory; the softmax threads read their row of S, apply the causal
 // limit, keep a running maximum per row (raised only past 2^8, log2 domain,
-// so O is rescaled rarely) and write their weights, rounded to fp16, to
-// shared memory as P_g; then O_g += P_g V_j accumulates in tensor memory, and
-// one more MMA against a column of ones adds the row sum of those same
-// rounded weights beside O.  The MMA warp issues the scores of tile j + 1
-// before the products of tile j, so the tensor cores work on the next scores
-// while the softmax threads exponentiate.
+// so O is rescaled rarely), add their weights to the row sum in fp32 and
+// write them, rounded to fp16, back to tensor memory as P_g; then O_g += P_g V_j
+// accumulates in tensor memory with P_g read from there.  The MMA warp issues
+// the scores of tile j + 1 before the products of tile j, so the tensor cores
+// work on the next scores while the softmax threads exponentiate.
+//
+// The MMAs' shared-memory operand reads bound this kernel before the tensor
+// math does: per 16-element K step an MMA reads its A block (4 KB) and its B
+// block from shared memory, so P stays in tensor memory (read there by the
+// MMA), and the row sums are added on the CUDA cores rather than by another
+// MMA that would read P again.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -43,10 +48,12 @@ namespace {
 
 constexpr int QT = 128;          // rows per query tile (the MMA's M)
 constexpr int SOFTMAX_WARPS = 8;
-constexpr int LOAD_WARP = 8;
-constexpr int MMA_WARP = 9;
-constexpr int NTHREADS = 320;
-constexpr int NS = 3;            // K/V stages
+constexpr int LOAD_K_WARP = 8;
+constexpr int MMA_S_WARP = 9;     // issues the scores; owns the tensor memory
+constexpr int MMA_PV_WARP = 10;   // issues the products
+constexpr int LOAD_V_WARP = 11;
+constexpr int NTHREADS = 384;
+constexpr int NS = 4;            // K/V stages
 constexpr int TMEM_COLS = 512;
 constexpr float kRescaleLog2 = 8.0f;
 constexpr unsigned FULL = 0xffffffffu;
@@ -57,19 +64,16 @@ struct Cfg {
     static constexpr int HALVES = D / 64;               // 64-element halves of a row
     static constexpr int Q_BYTES = QT * D * 2;          // one query tile
     static constexpr int KV_BYTES = BN * D * 2;         // one K or V tile
-    static constexpr int P_BYTES = QT * BN * 2;         // one query tile's weights
     static constexpr int OFF_K = 2 * Q_BYTES;
     static constexpr int OFF_V = OFF_K + NS * KV_BYTES;
-    static constexpr int OFF_P = OFF_V + NS * KV_BYTES;
-    static constexpr int OFF_ONES = OFF_P + 2 * P_BYTES;
-    static constexpr int DATA = OFF_ONES + 16 * 128;    // + a 16-row block whose row 0 is ones
+    static constexpr int DATA = OFF_V + NS * KV_BYTES;
     static constexpr int SMEM = DATA + 1024;            // slack to align the base to 1024 bytes
-    // tensor memory: S of query tile g at columns g BN .. ; O of tile g at
-    // 2 BN + g OW, its D columns followed by the row sum (blocks 32-column
-    // aligned)
-    static constexpr int OW = D + 32;
+    // tensor memory (fp32 columns): S of query tile g at g BN, O of tile g at
+    // 2 BN + g D, and the fp16 weights P of tile g, two per column (token 2c
+    // in the low half of column c), at 2 BN + 2 D + g BN / 2
     static constexpr int COL_O = 2 * BN;
-    static_assert(COL_O + 2 * OW <= TMEM_COLS, "tensor memory columns");
+    static constexpr int COL_P = COL_O + 2 * D;
+    static_assert(COL_P + BN <= TMEM_COLS, "tensor memory columns");
     static_assert(SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -100,13 +104,13 @@ struct Params {
 struct Bars {
     unsigned long long k_full[NS];
     unsigned long long v_full[NS];
-    unsigned long long kv_empty[NS];
-    unsigned long long q_full;
+    unsigned long long k_empty[NS];
+    unsigned long long v_empty[NS];
     unsigned long long s_full[2];
     unsigned long long s_free[2];
     unsigned long long p_full[2];
     unsigned long long o_done[2];
-    unsigned long long mma_done;
+    unsigned long long mma_done[2];
     uint32_t tmem_base;
 };
 
@@ -133,6 +137,16 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t a, uint64_t b, ui
         "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(a), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u)
+        : "memory");
+}
+
+// The same with A in tensor memory: row m of A in lane m, 16-bit elements
+// two per column from a_tmem on.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc ? 1u : 0u)
         : "memory");
 }
 
@@ -166,6 +180,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t *v) {
         : PKV_R8(0), PKV_R8(8)
         : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        PKV_W8(0), PKV_W8(8), PKV_W8(16), PKV_W8(24)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
@@ -185,10 +206,36 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 // Bounded wait on an mbarrier phase by every lane of the warp (each lane
-// observes the completion itself); true on every lane only if it completed
-// for all of them, so loops exit together.
+// observes the completion itself; cheaper than one lane polling and a
+// broadcast when the phase has already completed); true on every lane only
+// if it completed for all of them, so the warp leaves its loops together.
 __device__ __forceinline__ bool wait_lanes(uint32_t bar, uint32_t parity, int *status) {
     return __all_sync(FULL, mbar_wait(bar, parity, status));
+}
+
+// Packed pairs of fp32 (Blackwell's two-wide FMA and add).
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
@@ -215,8 +262,8 @@ __device__ __forceinline__ uint32_t swz(int t, int c, int rows) {
 }
 
 template <int D>
-// Ten warps: two SM sub-partitions hold three of them, so 168 registers a
-// thread is the most that fits (each sub-partition has 16K).
+// Twelve warps, three per SM sub-partition: 168 registers a thread is the
+// most that fits (each sub-partition has 16K).
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const Params p) {
@@ -273,25 +320,60 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     const uint32_t s_k = smem_addr(sm + C::OFF_K);
     const uint32_t s_v = smem_addr(sm + C::OFF_V);
-    const uint32_t s_ones = smem_addr(sm + C::OFF_ONES);
     auto bar = [](unsigned long long &x) { return smem_addr(&x); };
 
-    if (warp == MMA_WARP) {
+    // Softmax threads: their row, and the query row into shared memory
+    // (zeros past the last row) before the setup barrier, which then orders
+    // it before the first MMA.
+    const int g = (warp / 4) & 1;
+    const int t = (int)threadIdx.x % 128;                    // row of the tile = tensor-memory lane
+    const int r = r0 + g * QT + t;
+    const bool valid = warp < SOFTMAX_WARPS && r < r_end;
+    const int i = valid ? r / p.gh : 0;
+    const int lim = valid ? base + i : pmax[g];                // last position this row sees
+    const size_t ob = valid ? ((size_t)(q0 + i) * p.n_q_heads + (size_t)h * p.gh + (r - i * p.gh)) * D : 0;
+    if (warp < SOFTMAX_WARPS) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ob);
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+            const uint4 x = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4 *>(sm + g * C::Q_BYTES + swz(t, c, QT)) = x;
+        }
+        fence_proxy_async_shared();
+    }
+    // Loaders: block id of box `lane` of tile j (pages of 16 tokens and
+    // more; boxes past the CTA's last position are not loaded), read two
+    // tiles ahead of its use and range-checked only when used.
+    const int32_t *bt_row = p.bt + (size_t)s * p.max_blocks;
+    const int box = p.box_rows;
+    auto n_boxes = [&](int j) { return min(BN / box, (p_max - j * BN) / box + 1); };
+    auto raw_id = [&](int j) {
+        return (p.block_size >= 16 && j < ntt && lane < n_boxes(j)) ? bt_row[(j * BN + lane * box) / p.block_size] : 0;
+    };
+    int id0 = 0, id1 = 0;
+    if (warp == LOAD_K_WARP || warp == LOAD_V_WARP) {
+        prefetch_tensormap(warp == LOAD_K_WARP ? &tmk : &tmv);
+        id0 = raw_id(0);
+        id1 = raw_id(1);
+    }
+
+    if (warp == MMA_S_WARP) {
         if (lane == 0) {
             const uint32_t kv_arrivals = p.block_size >= 16 ? 1u : 32u;
-            for (int i = 0; i < NS; ++i) {
-                mbar_init(bar(bars.k_full[i]), kv_arrivals);
-                mbar_init(bar(bars.v_full[i]), kv_arrivals);
-                mbar_init(bar(bars.kv_empty[i]), 1);
+            for (int k = 0; k < NS; ++k) {
+                mbar_init(bar(bars.k_full[k]), kv_arrivals);
+                mbar_init(bar(bars.v_full[k]), kv_arrivals);
+                mbar_init(bar(bars.k_empty[k]), 1);
+                mbar_init(bar(bars.v_empty[k]), 1);
             }
-            mbar_init(bar(bars.q_full), SOFTMAX_WARPS * 32);
-            for (int g = 0; g < 2; ++g) {
-                mbar_init(bar(bars.s_full[g]), 1);
-                mbar_init(bar(bars.s_free[g]), 128);
-                mbar_init(bar(bars.p_full[g]), 128);
-                mbar_init(bar(bars.o_done[g]), 1);
+            for (int u = 0; u < 2; ++u) {
+                mbar_init(bar(bars.s_full[u]), 1);
+                mbar_init(bar(bars.s_free[u]), 128);
+                mbar_init(bar(bars.p_full[u]), 128);
+                mbar_init(bar(bars.o_done[u]), 1);
             }
-            mbar_init(bar(bars.mma_done), 1);
+            mbar_init(bar(bars.mma_done[0]), 1);
+            mbar_init(bar(bars.mma_done[1]), 1);
             mbar_init_fence();
         }
         __syncwarp();
@@ -301,15 +383,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    if (warp == LOAD_WARP) {
-        // the ones block: row 0 all ones (fp16 1.0), rows 1-15 zeros -- the
-        // same in every swizzle position, so one 64-token block serves
-        // every K step of the row-sum product
-        uint4 *o = reinterpret_cast<uint4 *>(sm + C::OFF_ONES);
-        for (int i = lane; i < 128; i += 32)
-            o[i] = i < 8 ? make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u) : make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_shared();
-    }
     tc_before_sync();
     __syncthreads();
     tc_after_sync();
@@ -317,32 +390,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 
     if (warp < SOFTMAX_WARPS) {
         // ---------------------------------------------------------- softmax
-        const int g = warp / 4;
-        const int t = (int)threadIdx.x % 128;                // row of the tile = tensor-memory lane
-        const int r = r0 + g * QT + t;
-        const bool valid = r < r_end;
-        const int i = valid ? r / p.gh : 0;
-        const int lim = valid ? base + i : pmax[g];            // last position this row sees
-        // q / out element offset of this row
-        const size_t ob = valid ? ((size_t)(q0 + i) * p.n_q_heads + (size_t)h * p.gh + (r - i * p.gh)) * D : 0;
-        {
-            // the query row, zeros past the last row
-            uint8_t *qs = sm + g * C::Q_BYTES;
-            const uint4 *src = reinterpret_cast<const uint4 *>(p.q + ob);
-#pragma unroll
-            for (int c = 0; c < D / 8; ++c) {
-                const uint4 x = valid ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4 *>(qs + swz(t, c, QT)) = x;
-            }
-            fence_proxy_async_shared();
-            mbar_arrive(bar(bars.q_full));
-        }
         const uint32_t lane_off = (uint32_t)((warp % 4) * 32) << 16;
         const uint32_t t_s = tmem + lane_off + (uint32_t)(g * BN);
-        const uint32_t t_o = tmem + lane_off + (uint32_t)(C::COL_O + g * C::OW);
-        uint8_t *ps = sm + C::OFF_P + g * C::P_BYTES;
+        const uint32_t t_o = tmem + lane_off + (uint32_t)(C::COL_O + g * D);
+        const uint32_t t_p = tmem + lane_off + (uint32_t)(C::COL_P + g * (BN / 2));
         const float sl = p.scale_log2;
         float m = -INFINITY;                                   // reference maximum, log2 units
+        float l = 0.0f;                                        // sum of the weights
         bool ok = true;
         for (int j = 0; j < nt[g]; ++j) {
             if (!wait_lanes(bar(bars.s_full[g]), j & 1, p.status)) {
@@ -366,23 +420,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             }
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < BN; c += 4) {
+            for (int c = 0; c < BN; c += 8) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) mx[e] = fmaxf(mx[e], __uint_as_float(x[c + e]));
+                for (int e = 0; e < 4; ++e)
+                    mx[e] = max3(mx[e], __uint_as_float(x[c + 2 * e]), __uint_as_float(x[c + 2 * e + 1]));
             }
-            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * sl;   // scale > 0
+            const float mt = max3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl;   // scale > 0
             float f = 1.0f;
             const bool resc = mt > m + kRescaleLog2;
             if (resc) {
                 f = ex2(m - mt);                                // m = -inf gives 0
                 m = mt;
+                l *= f;
             }
+            // weights 2^(s sl - m); their sum two at a time
             const float nm = -m;
+            uint64_t ls[2] = {f2_pack(0.0f, 0.0f), f2_pack(0.0f, 0.0f)};
             uint32_t pk[BN / 2];
 #pragma unroll
-            for (int c = 0; c < BN / 2; ++c)
-                pk[c] = pack_half2(ex2(fmaf(__uint_as_float(x[2 * c]), sl, nm)),
-                                   ex2(fmaf(__uint_as_float(x[2 * c + 1]), sl, nm)));
+            for (int c = 0; c < BN / 2; ++c) {
+                const float w0 = ex2(fmaf(__uint_as_float(x[2 * c]), sl, nm));
+                const float w1 = ex2(fmaf(__uint_as_float(x[2 * c + 1]), sl, nm));
+                ls[c & 1] = f2_add(ls[c & 1], f2_pack(w0, w1));
+                pk[c] = pack_half2(w0, w1);
+            }
+            {
+                float a0, a1, b0, b1;
+                f2_unpack(ls[0], a0, a1);
+                f2_unpack(ls[1], b0, b1);
+                l += (a0 + a1) + (b0 + b1);
+            }
 
             // the previous product has finished reading P and adding to O
             if (j > 0) {
@@ -392,9 +459,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
                 tc_after_sync();
                 if (__any_sync(FULL, resc)) {
-                    // rescale O and its row sum (lanes without a new maximum scale by 1)
+                    // rescale O (lanes without a new maximum scale by 1)
 #pragma unroll 1
-                    for (int c0 = 0; c0 < D + 16; c0 += 16) {
+                    for (int c0 = 0; c0 < D; c0 += 16) {
                         uint32_t o[16];
                         tmem_ld16(t_o + c0, o);
                         tmem_ld_wait();
@@ -405,26 +472,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                     tmem_st_wait();
                 }
             }
-            // P row t: tokens 64a .. 64a + 63 in block a
+            // P row t into tensor memory
 #pragma unroll
-            for (int a = 0; a < BN / 64; ++a) {
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int c = a * 32 + k * 4;
-                    *reinterpret_cast<uint4 *>(ps + a * QT * 128 + t * 128 + ((k ^ (t & 7)) << 4)) =
-                        make_uint4(pk[c], pk[c + 1], pk[c + 2], pk[c + 3]);
-                }
-            }
-            fence_proxy_async_shared();
+            for (int q = 0; q < BN / 64; ++q) tmem_st32(t_p + q * 32, pk + q * 32);
+            tmem_st_wait();
             tc_before_sync();
             mbar_arrive(bar(bars.p_full[g]));
         }
         if (ok && nt[g] > 0 && wait_lanes(bar(bars.o_done[g]), (nt[g] - 1) & 1, p.status)) {
             tc_after_sync();
-            uint32_t lv[16];
-            tmem_ld16(t_o + D, lv);
-            tmem_ld_wait();
-            const float inv = 1.0f / __uint_as_float(lv[0]);
+            const float inv = 1.0f / l;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 16) {
                 uint32_t o[16];
@@ -452,131 +509,102 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-    } else if (warp == LOAD_WARP) {
-        // ----------------------------------------------------------- loader
+    } else if (warp == LOAD_K_WARP || warp == LOAD_V_WARP) {
+        // ---------------------------------------------------------- loaders
+        // one warp for K, one for V; a stage is refilled once the MMAs of
+        // the tile that used it (the scores for K, the products for V) are done
+        const bool is_v = warp == LOAD_V_WARP;
+        const CUtensorMap *map = is_v ? &tmv : &tmk;
+        unsigned long long *full = is_v ? bars.v_full : bars.k_full;
+        unsigned long long *empty = is_v ? bars.v_empty : bars.k_empty;
+        const uint32_t s_base = is_v ? s_v : s_k;
+        const __half *pool_base = is_v ? p.v_pool : p.k_pool;
         const int B = p.block_size;
-        const int32_t *bt_row = p.bt + (size_t)s * p.max_blocks;
         int issued = 0;
         for (int j = 0; j < ntt; ++j) {
             const int st = j % NS;
-            if (j >= NS && !wait_lanes(bar(bars.kv_empty[st]), ((j / NS) - 1) & 1, p.status)) break;
-            const int tok0 = j * BN;
-            const uint32_t kst = s_k + st * C::KV_BYTES, vst = s_v + st * C::KV_BYTES;
+            int id = id0;
+            id0 = id1;
+            id1 = raw_id(j + 2);
+            const uint32_t dst = s_base + st * C::KV_BYTES;
+            if (j >= NS && !wait_lanes(bar(empty[st]), ((j / NS) - 1) & 1, p.status)) break;
             if (B >= 16) {
-                // boxes of box_rows tokens inside one page; boxes past the
-                // CTA's last position are not loaded (those rows are masked,
-                // and the MMA warp zeroes the V rows)
-                const int box = p.box_rows;
-                const int nvalid = min(BN / box, (p_max - tok0) / box + 1);
-                if (lane == 0) {
-                    const uint32_t bytes = (uint32_t)nvalid * box * D * 2;
-                    mbar_arrive_expect_tx(bar(bars.k_full[st]), bytes);
-                    mbar_arrive_expect_tx(bar(bars.v_full[st]), bytes);
+                const int nb = n_boxes(j);
+                if (lane < nb && (id < 0 || id >= p.n_blocks)) {
+                    atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
+                    id = 0;
                 }
+                if (lane == 0) mbar_arrive_expect_tx(bar(full[st]), (uint32_t)nb * box * D * 2);
                 __syncwarp();
-                if (lane < nvalid) {
-                    const int tok = tok0 + lane * box;
-                    int id = bt_row[tok / B];
-                    if (id < 0 || id >= p.n_blocks) {
-                        atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
-                        id = 0;
-                    }
-                    const int row = (int)(p.layer_row0 + (long long)id * B + tok % B);
+                if (lane < nb) {
+                    const int row = (int)(p.layer_row0 + (long long)id * B + (j * BN + lane * box) % B);
 #pragma unroll
-                    for (int hf = 0; hf < C::HALVES; ++hf) {
-                        const uint32_t off = (uint32_t)(hf * BN + lane * box) * 128u;
-                        tma_load_4d_plain(kst + off, &tmk, 0, row, hf, h, bar(bars.k_full[st]));
-                        tma_load_4d_plain(vst + off, &tmv, 0, row, hf, h, bar(bars.v_full[st]));
-                    }
+                    for (int hf = 0; hf < C::HALVES; ++hf)
+                        tma_load_4d_plain(dst + (uint32_t)(hf * BN + lane * box) * 128u, map, 0, row, hf, h,
+                                          bar(full[st]));
                 }
             } else {
                 // one token per page: 16-byte cp.async per chunk into its
                 // swizzled place, then a proxy fence before the arrival
                 for (int tk = lane; tk < BN; tk += 32) {
-                    const int tok = tok0 + tk;
+                    const int tok = j * BN + tk;
                     if (tok > p_max) break;
-                    int id = bt_row[tok];
-                    if (id < 0 || id >= p.n_blocks) {
+                    int bid = bt_row[tok];
+                    if (bid < 0 || bid >= p.n_blocks) {
                         atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
-                        id = 0;
+                        bid = 0;
                     }
-                    const size_t src = ((size_t)(p.layer_row0 + id) * p.n_kv_heads + h) * D;
+                    const __half *src = pool_base + ((size_t)(p.layer_row0 + bid) * p.n_kv_heads + h) * D;
 #pragma unroll
-                    for (int c = 0; c < D / 8; ++c) {
-                        cp_async16_cg(kst + swz(tk, c, BN), p.k_pool + src + c * 8);
-                        cp_async16_cg(vst + swz(tk, c, BN), p.v_pool + src + c * 8);
-                    }
+                    for (int c = 0; c < D / 8; ++c) cp_async16_cg(dst + swz(tk, c, BN), src + c * 8);
                 }
                 asm volatile("cp.async.wait_all;" ::: "memory");
                 fence_proxy_async_shared();
-                mbar_arrive(bar(bars.k_full[st]));
-                mbar_arrive(bar(bars.v_full[st]));
+                mbar_arrive(bar(full[st]));
             }
             ++issued;
         }
         // copies still in flight (only after a wait ran out) land before the CTA exits
         if (B >= 16) {
-            for (int j = max(0, issued - NS); j < issued; ++j) {
-                wait_lanes(bar(bars.k_full[j % NS]), (j / NS) & 1, p.status);
-                wait_lanes(bar(bars.v_full[j % NS]), (j / NS) & 1, p.status);
-            }
+            for (int j = max(0, issued - NS); j < issued; ++j) wait_lanes(bar(full[j % NS]), (j / NS) & 1, p.status);
         }
-    } else {
-        // -------------------------------------------------------------- MMA
+    } else if (warp == MMA_S_WARP) {
+        // ------------------------------------------------- MMA: S = Q K^T
         constexpr uint32_t ID_S = idesc_f16(QT, BN, false);
-        constexpr uint32_t ID_PV = idesc_f16(QT, 64, true);
-        constexpr uint32_t ID_L = idesc_f16(QT, 16, false);
         const uint32_t s_q = smem_addr(sm);
-        const uint32_t s_p = smem_addr(sm + C::OFF_P);
-        auto issue_s = [&](int g, int j) {
-            const uint32_t a0 = s_q + g * C::Q_BYTES;
-            const uint32_t b0 = s_k + (j % NS) * C::KV_BYTES;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)
-                umma(tmem + g * BN, sdesc(a0 + (kk / 4) * QT * 128 + (kk % 4) * 32),
-                     sdesc(b0 + (kk / 4) * BN * 128 + (kk % 4) * 32), ID_S, kk > 0);
-            umma_commit(bar(bars.s_full[g]));
-        };
-        auto issue_pv = [&](int g, int j) {
-            const uint32_t a0 = s_p + g * C::P_BYTES;
-            const uint32_t v0 = s_v + (j % NS) * C::KV_BYTES;
-            const uint32_t to = tmem + C::COL_O + g * C::OW;
-#pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-                const uint64_t ad = sdesc(a0 + (kk / 4) * QT * 128 + (kk % 4) * 32);
-                const bool acc = j > 0 || kk > 0;
-#pragma unroll
-                for (int hf = 0; hf < C::HALVES; ++hf)
-                    umma(to + hf * 64, ad, sdesc(v0 + hf * BN * 128 + kk * 2048), ID_PV, acc);
-                umma(to + D, ad, sdesc(s_ones + (kk % 4) * 32), ID_L, acc);
-            }
-            umma_commit(bar(bars.o_done[g]));
-        };
-        bool ok = wait_lanes(bar(bars.q_full), 0, p.status) && wait_lanes(bar(bars.k_full[0]), 0, p.status);
-        if (ok) {
-            tc_after_sync();
-            if (lane == 0) {
-                for (int g = 0; g < 2; ++g)
-                    if (nt[g] > 0) issue_s(g, 0);
-            }
-        }
+        bool ok = true;
         for (int j = 0; ok && j < ntt; ++j) {
             const int st = j % NS;
-            // the next tile's scores, once its K is in and S has been read
-            if (j + 1 < ntt) {
-                if (!wait_lanes(bar(bars.k_full[(j + 1) % NS]), ((j + 1) / NS) & 1, p.status)) break;
-                for (int g = 0; g < 2 && ok; ++g) {
-                    if (j + 1 < nt[g]) {
-                        if (!wait_lanes(bar(bars.s_free[g]), j & 1, p.status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_after_sync();
-                        if (lane == 0) issue_s(g, j + 1);
-                    }
+            if (!wait_lanes(bar(bars.k_full[st]), (j / NS) & 1, p.status)) break;
+            for (int g = 0; g < 2; ++g) {
+                if (j >= nt[g]) continue;
+                // S of this query tile has been read (its previous tile)
+                if (j > 0 && !wait_lanes(bar(bars.s_free[g]), (j - 1) & 1, p.status)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
+                tc_after_sync();
+                if (lane == 0) {
+                    const uint32_t a0 = s_q + g * C::Q_BYTES;
+                    const uint32_t b0 = s_k + st * C::KV_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma(tmem + g * BN, sdesc(a0 + (kk / 4) * QT * 128 + (kk % 4) * 32),
+                             sdesc(b0 + (kk / 4) * BN * 128 + (kk % 4) * 32), ID_S, kk > 0);
+                    umma_commit(bar(bars.s_full[g]));
+                }
             }
+            if (ok && lane == 0) umma_commit(bar(bars.k_empty[st]));
+        }
+        // every MMA issued has completed before tensor memory is released
+        if (lane == 0) umma_commit(bar(bars.mma_done[0]));
+        wait_lanes(bar(bars.mma_done[0]), 0, p.status);
+    } else {
+        // ------------------------------------------------ MMA: O += P V
+        constexpr uint32_t ID_PV = idesc_f16(QT, 64, true);
+        bool ok = true;
+        for (int j = 0; ok && j < ntt; ++j) {
+            const int st = j % NS;
             if (!wait_lanes(bar(bars.v_full[st]), (j / NS) & 1, p.status)) break;
             if (j == ntt - 1 && p_max - j * BN < BN - 1) {
                 // V rows past the CTA's last position: zeros (a zero weight
@@ -592,27 +620,36 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 fence_proxy_async_shared();
                 __syncwarp();
             }
-            for (int g = 0; g < 2 && ok; ++g) {
-                if (j < nt[g]) {
-                    if (!wait_lanes(bar(bars.p_full[g]), j & 1, p.status)) {
-                        ok = false;
-                        break;
+            for (int g = 0; g < 2; ++g) {
+                if (j >= nt[g]) continue;
+                if (!wait_lanes(bar(bars.p_full[g]), j & 1, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_after_sync();
+                if (lane == 0) {
+                    const uint32_t a0 = tmem + C::COL_P + g * (BN / 2);
+                    const uint32_t v0 = s_v + st * C::KV_BYTES;
+                    const uint32_t to = tmem + C::COL_O + g * D;
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+#pragma unroll
+                        for (int hf = 0; hf < C::HALVES; ++hf)
+                            umma_ts(to + hf * 64, a0 + kk * 8, sdesc(v0 + hf * BN * 128 + kk * 2048), ID_PV,
+                                    j > 0 || kk > 0);
                     }
-                    tc_after_sync();
-                    if (lane == 0) issue_pv(g, j);
+                    umma_commit(bar(bars.o_done[g]));
                 }
             }
-            if (!ok) break;
-            if (lane == 0) umma_commit(bar(bars.kv_empty[st]));
+            if (ok && lane == 0) umma_commit(bar(bars.v_empty[st]));
         }
-        // every MMA issued has completed before tensor memory is released
-        if (lane == 0) umma_commit(bar(bars.mma_done));
-        wait_lanes(bar(bars.mma_done), 0, p.status);
+        if (lane == 0) umma_commit(bar(bars.mma_done[1]));
+        wait_lanes(bar(bars.mma_done[1]), 0, p.status);
     }
 
     tc_before_sync();
     __syncthreads();
-    if (warp == MMA_WARP) {
+    if (warp == MMA_S_WARP) {
         tc_after_sync();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "n"(TMEM_COLS)
                      : "memory");
