@@ -222,11 +222,6 @@ __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
 __device__ __forceinline__ void f2_unpack(uint64_t v, float &lo, float &hi) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
 __device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
     uint64_t d;
     asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
@@ -350,22 +345,83 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto raw_id = [&](int j) {
         return (p.block_size >= 16 && j < ntt && lane < n_boxes(j)) ? bt_row[(j * BN + lane * box) / p.block_size] : 0;
     };
+    // Loaders (one warp for K, one for V; a stage is refilled once the MMAs
+    // of the tile that used it -- the scores for K, the products for V --
+    // are done).  Each initialises its own barriers and stages tile 0 before
+    // the setup barrier, so the first tiles arrive while the query rows load.
+    const bool loader = warp == LOAD_K_WARP || warp == LOAD_V_WARP;
+    const bool is_v = warp == LOAD_V_WARP;
+    const CUtensorMap *map = is_v ? &tmv : &tmk;
+    unsigned long long *full = is_v ? bars.v_full : bars.k_full;
+    unsigned long long *empty = is_v ? bars.v_empty : bars.k_empty;
+    const uint32_t s_base = is_v ? s_v : s_k;
+    const __half *pool_base = is_v ? p.v_pool : p.k_pool;
+    const int B = p.block_size;
+    int issued = 0;
+    // tile j into its stage (box `lane` from block id `id`); false if a wait ran out
+    auto load_tile = [&](int j, int id) -> bool {
+        const int st = j % NS;
+        const uint32_t dst = s_base + st * C::KV_BYTES;
+        if (j >= NS && !wait_lanes(bar(empty[st]), ((j / NS) - 1) & 1, p.status)) return false;
+        if (B >= 16) {
+            const int nb = n_boxes(j);
+            if (lane < nb && (id < 0 || id >= p.n_blocks)) {
+                atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
+                id = 0;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(bar(full[st]), (uint32_t)nb * box * D * 2);
+            __syncwarp();
+            if (lane < nb) {
+                const int row = (int)(p.layer_row0 + (long long)id * B + (j * BN + lane * box) % B);
+#pragma unroll
+                for (int hf = 0; hf < C::HALVES; ++hf)
+                    tma_load_4d_plain(dst + (uint32_t)(hf * BN + lane * box) * 128u, map, 0, row, hf, h, bar(full[st]));
+            }
+        } else {
+            // one token per page: 16-byte cp.async per chunk into its
+            // swizzled place, then a proxy fence before the arrival
+            for (int tk = lane; tk < BN; tk += 32) {
+                const int tok = j * BN + tk;
+                if (tok > p_max) break;
+                int bid = bt_row[tok];
+                if (bid < 0 || bid >= p.n_blocks) {
+                    atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
+                    bid = 0;
+                }
+                const __half *src = pool_base + ((size_t)(p.layer_row0 + bid) * p.n_kv_heads + h) * D;
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c) cp_async16_cg(dst + swz(tk, c, BN), src + c * 8);
+            }
+            asm volatile("cp.async.wait_all;" ::: "memory");
+            fence_proxy_async_shared();
+            mbar_arrive(bar(full[st]));
+        }
+        ++issued;
+        return true;
+    };
     int id0 = 0, id1 = 0;
-    if (warp == LOAD_K_WARP || warp == LOAD_V_WARP) {
-        prefetch_tensormap(warp == LOAD_K_WARP ? &tmk : &tmv);
+    if (loader) {
+        if (lane == 0) {
+            for (int k = 0; k < NS; ++k) {
+                mbar_init(bar(full[k]), B >= 16 ? 1u : 32u);
+                mbar_init(bar(empty[k]), 1);
+            }
+            mbar_init_fence();
+        }
+        __syncwarp();
+        prefetch_tensormap(map);
         id0 = raw_id(0);
         id1 = raw_id(1);
+        if (B >= 16) {
+            const int id = id0;
+            id0 = id1;
+            id1 = raw_id(2);
+            load_tile(0, id);
+        }
     }
 
     if (warp == MMA_S_WARP) {
         if (lane == 0) {
-            const uint32_t kv_arrivals = p.block_size >= 16 ? 1u : 32u;
-            for (int k = 0; k < NS; ++k) {
-                mbar_init(bar(bars.k_full[k]), kv_arrivals);
-                mbar_init(bar(bars.v_full[k]), kv_arrivals);
-                mbar_init(bar(bars.k_empty[k]), 1);
-                mbar_init(bar(bars.v_empty[k]), 1);
-            }
             for (int u = 0; u < 2; ++u) {
                 mbar_init(bar(bars.s_full[u]), 1);
                 mbar_init(bar(bars.s_free[u]), 128);
@@ -509,60 +565,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 }
             }
         }
-    } else if (warp == LOAD_K_WARP || warp == LOAD_V_WARP) {
+    } else if (loader) {
         // ---------------------------------------------------------- loaders
-        // one warp for K, one for V; a stage is refilled once the MMAs of
-        // the tile that used it (the scores for K, the products for V) are done
-        const bool is_v = warp == LOAD_V_WARP;
-        const CUtensorMap *map = is_v ? &tmv : &tmk;
-        unsigned long long *full = is_v ? bars.v_full : bars.k_full;
-        unsigned long long *empty = is_v ? bars.v_empty : bars.k_empty;
-        const uint32_t s_base = is_v ? s_v : s_k;
-        const __half *pool_base = is_v ? p.v_pool : p.k_pool;
-        const int B = p.block_size;
-        int issued = 0;
-        for (int j = 0; j < ntt; ++j) {
-            const int st = j % NS;
+        for (int j = issued; j < ntt; ++j) {
             int id = id0;
             id0 = id1;
             id1 = raw_id(j + 2);
-            const uint32_t dst = s_base + st * C::KV_BYTES;
-            if (j >= NS && !wait_lanes(bar(empty[st]), ((j / NS) - 1) & 1, p.status)) break;
-            if (B >= 16) {
-                const int nb = n_boxes(j);
-                if (lane < nb && (id < 0 || id >= p.n_blocks)) {
-                    atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
-                    id = 0;
-                }
-                if (lane == 0) mbar_arrive_expect_tx(bar(full[st]), (uint32_t)nb * box * D * 2);
-                __syncwarp();
-                if (lane < nb) {
-                    const int row = (int)(p.layer_row0 + (long long)id * B + (j * BN + lane * box) % B);
-#pragma unroll
-                    for (int hf = 0; hf < C::HALVES; ++hf)
-                        tma_load_4d_plain(dst + (uint32_t)(hf * BN + lane * box) * 128u, map, 0, row, hf, h,
-                                          bar(full[st]));
-                }
-            } else {
-                // one token per page: 16-byte cp.async per chunk into its
-                // swizzled place, then a proxy fence before the arrival
-                for (int tk = lane; tk < BN; tk += 32) {
-                    const int tok = j * BN + tk;
-                    if (tok > p_max) break;
-                    int bid = bt_row[tok];
-                    if (bid < 0 || bid >= p.n_blocks) {
-                        atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
-                        bid = 0;
-                    }
-                    const __half *src = pool_base + ((size_t)(p.layer_row0 + bid) * p.n_kv_heads + h) * D;
-#pragma unroll
-                    for (int c = 0; c < D / 8; ++c) cp_async16_cg(dst + swz(tk, c, BN), src + c * 8);
-                }
-                asm volatile("cp.async.wait_all;" ::: "memory");
-                fence_proxy_async_shared();
-                mbar_arrive(bar(full[st]));
-            }
-            ++issued;
+            if (!load_tile(j, id)) break;
         }
         // copies still in flight (only after a wait ran out) land before the CTA exits
         if (B >= 16) {
@@ -599,7 +608,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // every MMA issued has completed before tensor memory is released
         if (lane == 0) umma_commit(bar(bars.mma_done[0]));
         wait_lanes(bar(bars.mma_done[0]), 0, p.status);
-    } else {
+    } else if (warp == MMA_PV_WARP) {
         // ------------------------------------------------ MMA: O += P V
         constexpr uint32_t ID_PV = idesc_f16(QT, 64, true);
         bool ok = true;
