@@ -628,6 +628,21 @@ def run_ours(args, dist):
         pr_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*pr_args)), 10)
         pr_flops = 4.0 * Hq * D * Sp * Lp * (Lp + 1) / 2        # q.k and p.v over every causal pair
         del q_app, o_app, q_pr, o_pr
+        # the same prompts with grouped heads at head_dim 128 (32 q-heads over
+        # 8 kv-heads), on a pool of its own
+        gq_Hq, gq_Hkv, gq_D = 32, 8, 128
+        gq_nb = Sp * Lp // B
+        gq_k = torch.randn((1, gq_nb, B, gq_Hkv, gq_D), device=device).half()
+        gq_v = torch.randn((1, gq_nb, B, gq_Hkv, gq_D), device=device).half()
+        gq_pool = pkv.pf_pool_create(gq_k, gq_v)
+        gq_bt = to(np.random.default_rng(si.SEED_SHUFFLE).permutation(gq_nb).astype(np.int32).reshape(Sp, Lp // B))
+        gq_q = torch.randn((Sp * Lp, gq_Hq, gq_D), device=device).half()
+        gq_o = torch.empty_like(gq_q)
+        gq_args = (gq_pool.handle, 0, P(gq_q), P(gq_bt), Lp // B, P(pr_lens), P(pr_cu), Sp, Lp, gq_Hq,
+                   ctypes.c_float(1.0 / np.sqrt(gq_D)), P(gq_o), pkv.PF_F16, None, 0, sp)
+        gq_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*gq_args)), 10)
+        gq_flops = 4.0 * gq_Hq * gq_D * Sp * Lp * (Lp + 1) / 2
+        del gq_k, gq_v, gq_pool, gq_q, gq_o
 
         # grouped heads: 14 q-heads over 2 kv-heads x 64, 256 sequences of
         # U[32, 4096] tokens (each K/V byte serves 7 q-heads), attention alone
@@ -782,9 +797,14 @@ def run_ours(args, dist):
                                "tflops": round(pr_flops / (pr_ms / 1e3) / 1e12, 2), "bound": "tensor",
                                "peak_tflops": tc_peak,
                                "frac": round(pr_flops / (pr_ms / 1e3) / 1e12 / tc_peak, 4),
-                               "kernel": "prefill_mma_kernel<64> (mma.sync m16n8k16 fp16, fp32 accumulate)",
+                               "kernel": "prefill_tc_kernel<64> (tcgen05.mma, fp32 accumulators in tensor memory)",
                                "peak_note": f"{tc_src} dense bf16 burst TFLOP/s (MEASURED_PEAKS.json bf16_tflops; fp16 "
                                             "has the same nominal rate)"},
+            "prompt_prefill_gqa128": {"prompts": Sp, "tokens": Lp, "q_heads": gq_Hq, "kv_heads": gq_Hkv,
+                                      "head_dim": gq_D, "ms": round(gq_ms, 4), "flops": gq_flops,
+                                      "tflops": round(gq_flops / (gq_ms / 1e3) / 1e12, 2), "bound": "tensor",
+                                      "frac": round(gq_flops / (gq_ms / 1e3) / 1e12 / tc_peak, 4),
+                                      "kernel": "prefill_tc_kernel<128>"},
             "gqa_attention": {"workload": "256 sequences of U[32,4096] tokens, 14 q-heads / 2 kv-heads x 64, "
                                           "block 16, shuffled frames", "kernel": "paged_decode_kernel_mma_r128<64,8,2> "
                                           "(7 rows per kv-head on tensor cores)", "ms": round(gqa_ms, 5), "bytes": gqa_bytes,

@@ -1,7 +1,7 @@
 // prefill_tc.cu -- prompt attention through the block tables on the
-// fifth-generation tensor cores: tcgen05.mma with both operands in shared
-// memory and fp32 accumulators in tensor memory (pf_paged_prefill_attention
-// calls with 128 or more query rows per (sequence, kv-head)).
+// fifth-generation tensor cores: tcgen05.mma with fp32 accumulators in
+// tensor memory (pf_paged_prefill_attention calls with 128 or more query
+// rows per (sequence, kv-head)).
 //
 // Sequence s has L_s tokens, the last n_s of them new (PagedAttention blog,
 // "Architecture": append into the last block, then attend); the query of new
@@ -10,29 +10,35 @@
 // r = i * gh + g.
 //
 // A CTA serves 256 consecutive rows of one (sequence, kv-head) as two query
-// tiles of 128 rows (the MMA's M), with ten warps:
+// tiles of 128 rows (the MMA's M), with twelve warps:
 //   warps 0-3 and 4-7  the softmax of query tile 0 and 1: thread t owns row t
 //                      of its tile, which is lane t of tensor memory;
-//   warp 8             the loader: K and V tiles of BN tokens (128 at
+//   warps 8 and 11     the loaders of K and of V: tiles of BN tokens (128 at
 //                      head_dim 64, 64 at 128) through the block table into
-//                      a ring of four stages, by TMA boxes of whole pages
-//                      (block size 16 and up) or 16-byte cp.async per token
-//                      (block size 1), in the 128-byte swizzled layout;
-//   warp 9             owns the tensor memory; its lane 0 issues the MMAs.
-// Per K/V tile j and query tile g the MMA warp computes S_g = Q_g K_j^T into
-// tensor memory; the softmax threads read their row of S, apply the causal
-// limit, keep a running maximum per row (raised only past 2^8, log2 domain,
-// so O is rescaled rarely), add their weights to the row sum in fp32 and
-// write them, rounded to fp16, back to tensor memory as P_g; then O_g += P_g V_j
-// accumulates in tensor memory with P_g read from there.  The MMA warp issues
-// the scores of tile j + 1 before the products of tile j, so the tensor cores
-// work on the next scores while the softmax threads exponentiate.
+//                      a ring of four stages in the 128-byte swizzle, by TMA
+//                      boxes of up to a page (block size 16 and up) or
+//                      16-byte cp.async per token (block size 1);
+//   warp 9             issues the scores S_g = Q_g K_j^T (A and B in shared
+//                      memory) and owns the tensor memory;
+//   warp 10            issues the products O_g += P_g V_j (P in tensor
+//                      memory, V in shared memory).
+// The softmax threads read their row of S, apply the causal limit, keep a
+// running maximum per row (raised only past 2^8, log2 domain, so O is
+// rescaled rarely), add their weights to the row sum in fp32 and write them,
+// rounded to fp16, back to tensor memory as P_g.  Scores and products are
+// issued by separate warps so that one's waits leave the tensor pipe to the
+// other; with four stages the scores of the next tiles are computed while
+// the softmax threads exponentiate.
 //
-// The MMAs' shared-memory operand reads bound this kernel before the tensor
-// math does: per 16-element K step an MMA reads its A block (4 KB) and its B
-// block from shared memory, so P stays in tensor memory (read there by the
-// MMA), and the row sums are added on the CUDA cores rather than by another
-// MMA that would read P again.
+// Measured bounds (GB300, clock64 traces and single-CTA microbenchmarks of
+// tcgen05.mma kind::f16, M = 128, K = 16): one MMA costs about 100 cycles
+// with A and B in shared memory at N = 128 and about 71 with A in tensor
+// memory at N = 64 or 128 -- so P lives in tensor memory and the row sums
+// are summed on the CUDA cores rather than by another MMA over P.  A K/V
+// step of head_dim 64 (24 MMAs) then takes about 2,400 cycles, about the
+// rate at which the TMA unit delivers a tile pair of 128-byte page rows
+// (about 15 bytes a cycle per SM); 16-byte cp.async from two warps was several
+// times slower still.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 

@@ -159,3 +159,31 @@ def test_short_append_large_batch(pkv, cuda_dev, oracle_mod):
     q, cu, got = _run_ws(pkv, cuda_dev, c, n_new, 0.125)
     ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, 0.125)
     assert_close_to_oracle(got, ref, what="append, 1500 sequences")
+
+
+@pytest.mark.parametrize("d,b", [(64, 16), (128, 64)])
+def test_prompt_with_growing_scores_rescales(pkv, cuda_dev, oracle_mod, d, b):
+    """Keys that grow along the prompt in the queries' direction raise every
+    row's running maximum by far more than 2^8 from one K/V tile to the next,
+    so the accumulated output in tensor memory is rescaled at nearly every
+    tile; the result still matches the oracle."""
+    import torch
+    lens = np.array([900, 513, 130], dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 4, 2, d, b)
+    u = np.full(d, 1.0 / np.sqrt(d), dtype=np.float32)          # unit direction
+    for s, L in enumerate(lens):
+        for t in range(L):
+            blk, row = c.bt[s, t // b], t % b
+            k = c.k_host[0, blk, row].astype(np.float32) * 0.1 + u * (t / 4.0)
+            c.k_host[0, blk, row] = k.astype(np.float16)
+    c.k_dev.copy_(torch.from_numpy(c.k_host))
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = (si.fp16_normal((int(cu[-1]), 4, d), 501).astype(np.float32) * 0.1 + 4.0 * u).astype(np.float16)
+    scale = float(np.float32(1.0 / np.sqrt(d)))
+    out = torch.full((int(cu[-1]), 4, d), float("nan"), dtype=torch.float16, device=cuda_dev)
+    pkv.pf_paged_prefill_attention(c.pool, 0, dev(q, cuda_dev), c.bt_dev, c.lens_dev, dev(cu, cuda_dev),
+                                   int(lens.max()), scale, out)
+    torch.cuda.synchronize()
+    ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, np.float32(scale))
+    assert_close_to_oracle(host(out), ref, what=f"growing scores d={d}")
+    assert pkv.pf_device_status(reset=True) == 0
