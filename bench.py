@@ -70,6 +70,9 @@ def parse_args(argv=None):
                    help="write profiles/<--profile-name>.json from `ncu -i REP --page raw --csv` output, then exit")
     p.add_argument("--profile-name", default="attention_mixed_shuffled")
     p.add_argument("--profile-command", default="", help="the ncu command the capture came from (recorded)")
+    p.add_argument("--prompt-only", action="store_true",
+                   help="time only the prompt-attention legs on pools of their own (a small device footprint, "
+                        "for profiling); prints one diagnostic JSON line, not the bench line")
     return p.parse_args(argv)
 
 
@@ -1002,8 +1005,58 @@ def run_reference(args, dist):
     }
 
 
+def run_prompt_only(args):
+    """The prompt legs alone: 4 prompts of 2048 tokens, 12 heads x 64 and 32
+    q-heads over 8 kv-heads x 128, pages of 16 tokens in shuffled frames, each
+    on a pool holding just those pages (a few tens of MB on the device)."""
+    import numpy as np
+    import torch
+    import paged_kv_cache_37_gb300 as pkv
+    pkv.lib()
+    device = torch.device("cuda", 0)
+    tc_peak, tc_src = read_tensor_peak()
+    Sp, Lp, B = 4, 2048, 16
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)
+    lens = to(np.full(Sp, Lp, dtype=np.int32))
+    cu = to(np.arange(Sp + 1, dtype=np.int32) * Lp)
+    out = {"mode": "prompt_only", "prompts": Sp, "tokens": Lp, "block_size": B}
+    for name, Hq, Hkv, D in (("prompt_prefill", 12, 12, 64), ("prompt_prefill_gqa128", 32, 8, 128)):
+        nb = Sp * Lp // B
+        gen = torch.Generator(device=device).manual_seed(si.SEED_VALUES)
+        k = torch.randn((1, nb, B, Hkv, D), generator=gen, device=device).half()
+        v = torch.randn((1, nb, B, Hkv, D), generator=gen, device=device).half()
+        pool = pkv.pf_pool_create(k, v)
+        bt = to(np.random.default_rng(si.SEED_SHUFFLE).permutation(nb).astype(np.int32).reshape(Sp, Lp // B))
+        q = torch.randn((Sp * Lp, Hq, D), generator=gen, device=device).half()
+        o = torch.empty_like(q)
+        call = lambda: pkv.pf_paged_prefill_attention(pool, 0, q, bt, lens, cu, Lp, 1.0 / np.sqrt(D), o)
+        for _ in range(max(args.warmup, 3)):
+            call()
+        torch.cuda.synchronize(device)
+        n = max(1, min(args.steps, 200))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            call()
+        e1.record()
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / n
+        flops = 4.0 * Hq * D * Sp * Lp * (Lp + 1) / 2
+        tf = flops / (ms / 1e3) / 1e12
+        out[name] = {"q_heads": Hq, "kv_heads": Hkv, "head_dim": D, "calls": n, "ms": round(ms, 4),
+                     "tflops": round(tf, 2), "frac": round(tf / tc_peak, 4), "peak_tflops": tc_peak,
+                     "peak_source": tc_src}
+        del k, v, pool, q, o
+    if pkv.pf_device_status(reset=True) != 0:
+        raise RuntimeError("device status flagged during the prompt legs")
+    return out
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.prompt_only:
+        print(json.dumps(run_prompt_only(args)), flush=True)
+        return
     if args.record_traffic:
         print(record_traffic(args.record_traffic, args.profile_name, args.profile_command))
         return
