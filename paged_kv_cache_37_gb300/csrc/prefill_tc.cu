@@ -10,18 +10,21 @@
 // r = i * gh + g.
 //
 // A CTA serves 256 consecutive rows of one (sequence, kv-head) as two query
-// tiles of 128 rows (the MMA's M), with twelve warps:
+// tiles of 128 rows (the MMA's M), with sixteen warps:
 //   warps 0-3 and 4-7  the softmax of query tile 0 and 1: thread t owns row t
 //                      of its tile, which is lane t of tensor memory;
-//   warps 8 and 11     the loaders of K and of V: tiles of BN tokens (128 at
-//                      head_dim 64, 64 at 128) through the block table into
-//                      a ring of four stages in the 128-byte swizzle, by TMA
-//                      boxes of up to a page (block size 16 and up) or
-//                      16-byte cp.async per token (block size 1);
-//   warp 9             issues the scores S_g = Q_g K_j^T (A and B in shared
+//   warps 8-11         the loaders, two for K and two for V: tiles of BN
+//                      tokens (128 at head_dim 64, 64 at 128) through the
+//                      block table into a ring of four stages in the
+//                      128-byte swizzle, by TMA boxes of up to a page (block
+//                      size 16 and up; each warp every other box) or 16-byte
+//                      cp.async per token (block size 1);
+//   warp 12            issues the scores S_g = Q_g K_j^T (A and B in shared
 //                      memory) and owns the tensor memory;
-//   warp 10            issues the products O_g += P_g V_j (P in tensor
-//                      memory, V in shared memory).
+//   warp 13            issues the products O_g += P_g V_j (P in tensor
+//                      memory, V in shared memory); warps 14-15 idle.
+// The softmax warpgroups run with 200 registers a thread, the others with
+// 56 (setmaxnreg after the setup barrier).
 // The softmax threads read their row of S, apply the causal limit, keep a
 // running maximum per row (raised only past 2^8, log2 domain, so O is
 // rescaled rarely), add their weights to the row sum in fp32 and write them,
@@ -53,12 +56,19 @@ namespace prefill_tc {
 namespace {
 
 constexpr int QT = 128;          // rows per query tile (the MMA's M)
-constexpr int SOFTMAX_WARPS = 8;
-constexpr int LOAD_K_WARP = 8;
-constexpr int MMA_S_WARP = 9;     // issues the scores; owns the tensor memory
-constexpr int MMA_PV_WARP = 10;   // issues the products
-constexpr int LOAD_V_WARP = 11;
-constexpr int NTHREADS = 384;
+constexpr int SOFTMAX_WARPS = 8;  // warpgroups 0 and 1
+constexpr int LOAD_WARP0 = 8;     // warpgroup 2: K loaders (warps 8, 9), V loaders (10, 11)
+constexpr int MMA_S_WARP = 12;    // warpgroup 3: issues the scores; owns the tensor memory
+constexpr int MMA_PV_WARP = 13;   // issues the products (warps 14 and 15 idle)
+constexpr int NTHREADS = 512;
+// Registers: launched at 128 a thread (512 threads, one CTA per SM); the
+// loader and MMA warpgroups then give theirs down to REG_OTHER and the
+// softmax warpgroups take REG_SOFTMAX.  Each SM sub-partition holds one warp
+// of every warpgroup, so the split must also fit its 16K registers.
+constexpr int REG_SOFTMAX = 200;
+constexpr int REG_OTHER = 56;
+static_assert(2 * 128 * REG_SOFTMAX + 2 * 128 * REG_OTHER == NTHREADS * 128, "the split is the launch's registers");
+static_assert(32 * (2 * REG_SOFTMAX + 2 * REG_OTHER) <= 16384, "a sub-partition's registers");
 constexpr int NS = 4;            // K/V stages
 constexpr int TMEM_COLS = 512;
 constexpr float kRescaleLog2 = 8.0f;
@@ -263,8 +273,6 @@ __device__ __forceinline__ uint32_t swz(int t, int c, int rows) {
 }
 
 template <int D>
-// Twelve warps, three per SM sub-partition: 168 registers a thread is the
-// most that fits (each sub-partition has 16K).
 __global__ void __launch_bounds__(NTHREADS, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
                       const Params p) {
@@ -351,12 +359,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     auto raw_id = [&](int j) {
         return (p.block_size >= 16 && j < ntt && lane < n_boxes(j)) ? bt_row[(j * BN + lane * box) / p.block_size] : 0;
     };
-    // Loaders (one warp for K, one for V; a stage is refilled once the MMAs
-    // of the tile that used it -- the scores for K, the products for V --
-    // are done).  Each initialises its own barriers and stages tile 0 before
-    // the setup barrier, so the first tiles arrive while the query rows load.
-    const bool loader = warp == LOAD_K_WARP || warp == LOAD_V_WARP;
-    const bool is_v = warp == LOAD_V_WARP;
+    // Loaders (two warps for K, two for V, each issuing every other page
+    // box of a tile; a stage is refilled once the MMAs of the tile that used
+    // it -- the scores for K, the products for V -- are done).  They set up
+    // their barriers and stage tile 0 before the setup barrier, so the first
+    // tiles arrive while the query rows load.
+    const bool loader = warp >= LOAD_WARP0 && warp < LOAD_WARP0 + 4;
+    const bool is_v = warp >= LOAD_WARP0 + 2;
+    const int li = (warp - LOAD_WARP0) & 1;                  // this warp's boxes: lane % 2 == li
     const CUtensorMap *map = is_v ? &tmv : &tmk;
     unsigned long long *full = is_v ? bars.v_full : bars.k_full;
     unsigned long long *empty = is_v ? bars.v_empty : bars.k_empty;
@@ -371,13 +381,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         if (j >= NS && !wait_lanes(bar(empty[st]), ((j / NS) - 1) & 1, p.status)) return false;
         if (B >= 16) {
             const int nb = n_boxes(j);
-            if (lane < nb && (id < 0 || id >= p.n_blocks)) {
+            const bool mine = lane < nb && (lane & 1) == li;
+            if (mine && (id < 0 || id >= p.n_blocks)) {
                 atomicOr(p.status, PF_DEV_BAD_BLOCK_ID);
                 id = 0;
             }
-            if (lane == 0) mbar_arrive_expect_tx(bar(full[st]), (uint32_t)nb * box * D * 2);
+            if (lane == 0) mbar_arrive_expect_tx(bar(full[st]), (uint32_t)((nb + 1 - li) / 2) * box * D * 2);
             __syncwarp();
-            if (lane < nb) {
+            if (mine) {
                 const int row = (int)(p.layer_row0 + (long long)id * B + (j * BN + lane * box) % B);
 #pragma unroll
                 for (int hf = 0; hf < C::HALVES; ++hf)
@@ -386,7 +397,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         } else {
             // one token per page: 16-byte cp.async per chunk into its
             // swizzled place, then a proxy fence before the arrival
-            for (int tk = lane; tk < BN; tk += 32) {
+            for (int tk = lane + 32 * li; tk < BN; tk += 64) {
                 const int tok = j * BN + tk;
                 if (tok > p_max) break;
                 int bid = bt_row[tok];
@@ -407,14 +418,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     };
     int id0 = 0, id1 = 0;
     if (loader) {
-        if (lane == 0) {
+        if (warp == LOAD_WARP0 && lane == 0) {
+            // two loader warps arrive on each full barrier
             for (int k = 0; k < NS; ++k) {
-                mbar_init(bar(full[k]), B >= 16 ? 1u : 32u);
-                mbar_init(bar(empty[k]), 1);
+                mbar_init(bar(bars.k_full[k]), B >= 16 ? 2u : 64u);
+                mbar_init(bar(bars.v_full[k]), B >= 16 ? 2u : 64u);
+                mbar_init(bar(bars.k_empty[k]), 1);
+                mbar_init(bar(bars.v_empty[k]), 1);
             }
             mbar_init_fence();
         }
-        __syncwarp();
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // the loader warps: barriers initialised
         prefetch_tensormap(map);
         id0 = raw_id(0);
         id1 = raw_id(1);
@@ -449,6 +463,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     __syncthreads();
     tc_after_sync();
     const uint32_t tmem = bars.tmem_base;
+    if (warp >= SOFTMAX_WARPS) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_OTHER));
+    else asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REG_SOFTMAX));
 
     if (warp < SOFTMAX_WARPS) {
         // ---------------------------------------------------------- softmax
