@@ -187,3 +187,43 @@ def test_prompt_with_growing_scores_rescales(pkv, cuda_dev, oracle_mod, d, b):
     ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, np.float32(scale))
     assert_close_to_oracle(host(out), ref, what=f"growing scores d={d}")
     assert pkv.pf_device_status(reset=True) == 0
+
+
+def test_prompt_kernel_flags_a_bad_block_id(pkv, cuda_dev, oracle_mod):
+    """A block id outside the pool in one prompt's table (on the tcgen05
+    kernel: 128+ rows per kv-head) is flagged and read as page 0: that
+    prompt's output stays finite, and the other prompt still matches the
+    oracle."""
+    import torch
+    lens = np.array([300, 200], dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 4, 2, 64, 16)
+    bt_bad = c.bt.copy()
+    bt_bad[0, 3] = c.n_blocks + 7
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    q = si.fp16_normal((int(cu[-1]), 4, 64), 502)
+    out = torch.full((int(cu[-1]), 4, 64), float("nan"), dtype=torch.float16, device=cuda_dev)
+    pkv.pf_device_status(reset=True)
+    pkv.pf_paged_prefill_attention(c.pool, 0, dev(q, cuda_dev), dev(bt_bad, cuda_dev), c.lens_dev, dev(cu, cuda_dev),
+                                   int(lens.max()), 0.125, out)
+    torch.cuda.synchronize()
+    assert pkv.pf_device_status(reset=True) & pkv.PF_DEV_BAD_BLOCK_ID
+    got = host(out)
+    assert np.all(np.isfinite(got))
+    ref = oracle_mod.prefill_attention(q, c.k_host, c.v_host, 0, c.bt, lens, cu, 0.125)
+    assert_close_to_oracle(got[cu[1]:], ref[cu[1]:], what="the other prompt")
+
+
+def test_prompt_kernel_flags_too_many_new_tokens(pkv, cuda_dev):
+    """More new tokens than a sequence holds, on the tcgen05 kernel: flagged,
+    clamped, and every output finite."""
+    import torch
+    lens = np.array([100, 300], dtype=np.int32)
+    c = PagedCase(pkv, cuda_dev, lens, 4, 4, 64, 16)
+    cu = np.array([0, 150, 450], dtype=np.int32)            # 150 new tokens in a 100-token sequence
+    q = dev(si.fp16_normal((450, 4, 64), 503), cuda_dev)
+    out = torch.zeros((450, 4, 64), dtype=torch.float16, device=cuda_dev)
+    pkv.pf_device_status(reset=True)
+    pkv.pf_paged_prefill_attention(c.pool, 0, q, c.bt_dev, c.lens_dev, dev(cu, cuda_dev), 300, 0.125, out)
+    torch.cuda.synchronize()
+    assert pkv.pf_device_status(reset=True) & pkv.PF_DEV_BAD_LENGTH
+    assert np.all(np.isfinite(host(out)))
