@@ -320,18 +320,21 @@ PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
  * the grid).  On the device, n_s > L or > max_new_tokens, or a length
  * outside the table, sets PF_DEV_BAD_LENGTH and is clamped; bad block ids set
  * PF_DEV_BAD_BLOCK_ID.
- * Two kernels: with a workspace (of pf_prefill_workspace_bytes bytes,
- * initialised once with pf_decode_workspace_init, not shared by overlapping
- * calls) and max_new_tokens x (n_q_heads / Hkv) <= 8 (16 on pages of at
- * least 16 tokens), the decode kernel serves the new tokens as extra rows of
- * each kv-head -- balanced spans over the contexts, every K/V byte read once
- * per kv-head (a chunked append); otherwise (workspace null, or longer
- * appends and prompts) a kernel that needs no workspace takes 64 query rows
- * (new tokens x q-heads) of one (sequence, kv-head) per block and walks the
- * context up to their last position.  Both compute the products on tensor
- * cores with the softmax weights rounded to fp16 (within the attention
- * tolerance).
- * Up to 16 q-heads per kv-head. */
+ * Three kernels, chosen by rows = max_new_tokens x (n_q_heads / Hkv):
+ * - with a workspace (of pf_prefill_workspace_bytes bytes, initialised once
+ *   with pf_decode_workspace_init, not shared by overlapping calls) and
+ *   rows <= 8 (16 on pages of at least 16 tokens), the decode kernel serves
+ *   the new tokens as extra rows of each kv-head -- balanced spans over the
+ *   contexts, every K/V byte read once per kv-head (a chunked append);
+ * - otherwise, with rows >= 128 (prompts, long appends), a kernel on the
+ *   fifth-generation tensor cores (tcgen05.mma, fp32 accumulators in tensor
+ *   memory) takes 256 query rows of one (sequence, kv-head) per block and
+ *   walks the context up to their last position; it needs no workspace;
+ * - otherwise a warp-level MMA kernel does the same with 64 rows per block.
+ * All compute the products on tensor cores with the softmax weights rounded
+ * to fp16 (within the attention tolerance).
+ * Up to 16 q-heads per kv-head; the tcgen05 kernel holds one block per SM
+ * (about 165 KB of shared memory and all 512 tensor-memory columns). */
 PF_API int pf_paged_prefill_attention(const pf_pool *pool, int layer,
                                       const void *q,
                                       const int32_t *block_tables,
