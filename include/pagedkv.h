@@ -334,7 +334,8 @@ PF_API int pf_decode_step(const pf_pool *pool, int layer, const void *q,
  * All compute the products on tensor cores with the softmax weights rounded
  * to fp16 (within the attention tolerance).
  * Up to 16 q-heads per kv-head; the tcgen05 kernel holds one block per SM
- * (about 165 KB of shared memory and all 512 tensor-memory columns). */
+ * (165 KB of shared memory at head_dim 64, 197 KB at 128, and all 512
+ * tensor-memory columns). */
 PF_API int pf_paged_prefill_attention(const pf_pool *pool, int layer,
                                       const void *q,
                                       const int32_t *block_tables,
