@@ -38,10 +38,12 @@
 // with A and B in shared memory at N = 128 and about 71 with A in tensor
 // memory at N = 64 or 128 -- so P lives in tensor memory and the row sums
 // are summed on the CUDA cores rather than by another MMA over P.  A K/V
-// step of head_dim 64 (24 MMAs) then takes about 2,400 cycles, about the
-// rate at which the TMA unit delivers a tile pair of 128-byte page rows
-// (about 15 bytes a cycle per SM); 16-byte cp.async from two warps was several
-// times slower still.
+// step of head_dim 64 (24 MMAs) then takes about 2,400 cycles.  TMA boxes
+// issued from one warp arrive at a few hundred cycles each whatever their
+// size, and the rate grows with the number of issuing warps (measured: 1, 2,
+// 4 warps -> 11.8, 23.4, 44 bytes a cycle per SM on 8 KB boxes), hence two
+// loader warps per tensor; 16-byte cp.async from the loader warps was several
+// times slower than TMA.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
