@@ -646,7 +646,7 @@ def run_ours(args, dist):
         o_pr = torch.empty_like(q_pr)
         pr_args = (reps[0]["pool"].handle, 0, P(q_pr), P(pr_bt), Lp // B, P(pr_lens), P(pr_cu), Sp, Lp, Hq,
                    ctypes.c_float(w["scale"]), P(o_pr), pkv.PF_F16, None, 0, sp)
-        pr_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*pr_args)), 10)
+        pr_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*pr_args)), 50)
         pr_flops = 4.0 * Hq * D * Sp * Lp * (Lp + 1) / 2        # q.k and p.v over every causal pair
         del q_app, o_app, q_pr, o_pr
         # the same prompts with grouped heads at head_dim 128 (32 q-heads over
@@ -661,7 +661,7 @@ def run_ours(args, dist):
         gq_o = torch.empty_like(gq_q)
         gq_args = (gq_pool.handle, 0, P(gq_q), P(gq_bt), Lp // B, P(pr_lens), P(pr_cu), Sp, Lp, gq_Hq,
                    ctypes.c_float(1.0 / np.sqrt(gq_D)), P(gq_o), pkv.PF_F16, None, 0, sp)
-        gq_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*gq_args)), 10)
+        gq_ms = time_calls(lambda i: check(lib.pf_paged_prefill_attention(*gq_args)), 50)
         gq_flops = 4.0 * gq_Hq * gq_D * Sp * Lp * (Lp + 1) / 2
         del gq_k, gq_v, gq_pool, gq_q, gq_o
 
