@@ -231,7 +231,7 @@ __device__ __forceinline__ bool wait_lanes(uint32_t bar, uint32_t parity, int *s
     return __all_sync(FULL, mbar_wait(bar, parity, status));
 }
 
-// Packed pairs of fp32 (Blackwell's two-wide FMA and add).
+// Packed pairs of fp32 for Blackwell's two-wide add.
 __device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
     uint64_t r;
     asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
