@@ -459,3 +459,38 @@ def test_prefill_is_causal(oracle_mod):
     k3[0, bt[0, page], off] = np.float16(7.0)
     out = oracle_mod.prefill_attention(q, k3, v, 0, bt, [L], [0, n], 0.125)
     assert all(not np.array_equal(out[i], base[i]) for i in range(n))
+
+
+@pytest.mark.parametrize("hq,hkv,d,B", [(4, 2, 64, 16), (6, 6, 32, 1), (8, 1, 128, 4)])
+def test_prefill_matches_torch_sdpa_with_a_causal_mask(oracle_mod, hq, hkv, d, B):
+    """The multi-token append against torch's fp64 scaled-dot-product
+    attention with an explicit mask: new token i of a sequence of L tokens (n
+    of them new) sits at position L - n + i and attends to positions 0 .. L - n
+    + i, through the block table; whole prompts, appends and a sequence with
+    no new token."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    lens = np.array([1, 9, 40, 23, 17], dtype=np.int32)
+    n_new = np.array([1, 9, 6, 0, 17], dtype=np.int32)
+    cu = np.concatenate([[0], np.cumsum(n_new)]).astype(np.int32)
+    n_blocks = int(sum(-(-int(L) // B) for L in lens)) + 5
+    bt = si.block_tables(lens, B, n_blocks, 61)
+    k = si.pool(1, n_blocks, B, hkv, d, 62)
+    v = si.pool(1, n_blocks, B, hkv, d, 63)
+    q = si.fp16_normal((int(cu[-1]), hq, d), 64)
+    scale = float(np.float32(1.0 / math.sqrt(d)))
+    ours = oracle_mod.prefill_attention(q, k, v, 0, bt, lens, cu, scale)
+    K = k.astype(np.float64)[0].reshape(-1, hkv, d)
+    V = v.astype(np.float64)[0].reshape(-1, hkv, d)
+    for s, (L, n) in enumerate(zip(lens, n_new)):
+        if n == 0:
+            continue
+        t = np.arange(L)
+        slots = bt[s, t // B].astype(np.int64) * B + t % B
+        ks = torch.from_numpy(K[slots]).permute(1, 0, 2)[None]                     # [1, Hkv, L, D]
+        vs = torch.from_numpy(V[slots]).permute(1, 0, 2)[None]
+        qs = torch.from_numpy(q[cu[s]:cu[s + 1]].astype(np.float64)).permute(1, 0, 2)[None]   # [1, Hq, n, D]
+        pos = L - n + np.arange(n)
+        mask = torch.from_numpy(t[None, :] <= pos[:, None])                        # [n, L], True = attended
+        ref = F.scaled_dot_product_attention(qs, ks, vs, attn_mask=mask, scale=scale, enable_gqa=(hq != hkv))
+        np.testing.assert_allclose(ours[cu[s]:cu[s + 1]], ref[0].permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
